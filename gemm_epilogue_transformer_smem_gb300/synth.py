@@ -1,0 +1,137 @@
+"""Seeded synthetic inputs for the five GEMM + epilogue workloads.
+
+This module holds shapes, value distributions and random draws only -- none
+of the method's arithmetic.  Both the CUDA path and the CPU oracle read the
+tensors it returns (the oracle through host copies of the same bf16 bits).
+
+Workloads (shapes and distributions as the benchmark configuration states
+them; "N(0, s)" has standard deviation s):
+
+  tiny      C = gelu_tanh(1.0 * A@B + bias), AMAX.  A 64x128, B 128x64, both
+            N(0,1)/sqrt(128); bias fp32 N(0, 0.1), length 64.
+  swiglu    MLP up-projection, out = silu(gate) * up on interleaved columns.
+            A 8192x4096 N(0,1); B 4096x28672 N(0, 0.02).
+  fp8       relu(0.5 * A@B + bias), AMAX, bf16 C and e4m3 C with scale 448/4.
+            M = N = K = 8192, A and B N(0,1)/sqrt(8192); bias N(0, 0.1).
+  downproj  out = residual + A@B, per-row rsqrt(mean(out^2) + 1e-6).
+            A 16384x14336 N(0,1)/sqrt(14336); B 14336x4096 N(0, 0.02);
+            residual 16384x4096 N(0,1).
+  backward  dX = (dY @ W^T) * gelu_tanh'(preact), column sums of dX.
+            dY 8192x4096 N(0,1); W 16384x4096 N(0, 0.02); preact 8192x16384
+            N(0,1).
+
+Draw order per workload: A, B, bias, residual / preact.  Each tensor is drawn
+in fp32 with ``torch.randn`` from one generator seeded with 1000 + index,
+scaled, then cast to bf16 (round to nearest even); bias stays fp32.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    M: int
+    N: int               # accumulator columns (B's N)
+    K: int
+    b_layout: str        # "kn": B stored K x N; "nk": B stored N x K (B = W^T)
+    program: tuple       # op names, oracle spelling; see api.PROGRAM_OPS
+    a_std: float
+    b_std: float
+    bias_std: Optional[float] = None
+    aux: Optional[str] = None       # "residual" or "preact"
+    aux_std: float = 1.0
+    alpha: float = 1.0
+    fp8_scale: float = 1.0
+    notes: str = ""
+
+    @property
+    def n_out(self) -> int:
+        return self.N // 2 if any(op.startswith("pair_swiglu") for op in self.program) else self.N
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def scaled(self, M: int, N: int, K: int, name: Optional[str] = None) -> "Workload":
+        """Same program and distributions at another shape.  Standard
+        deviations that the full workload ties to K (1/sqrt(K)) follow K."""
+        a_std, b_std = self.a_std, self.b_std
+        if self.name in ("tiny", "fp8", "downproj"):
+            a_std = 1.0 / math.sqrt(K)
+        if self.name in ("tiny", "fp8"):
+            b_std = 1.0 / math.sqrt(K)
+        return replace(self, name=name or "%s_%dx%dx%d" % (self.name, M, N, K), M=M, N=N, K=K,
+                       a_std=a_std, b_std=b_std)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 0, 64, 64, 128, "kn",
+                     ("alpha", "bias", "gelu_tanh", "amax", "store_bf16"),
+                     a_std=1 / math.sqrt(128), b_std=1 / math.sqrt(128), bias_std=0.1,
+                     alpha=1.0),
+    "swiglu": Workload("swiglu", 1, 8192, 28672, 4096, "kn",
+                       ("pair_swiglu", "store_bf16"),
+                       a_std=1.0, b_std=0.02),
+    "fp8": Workload("fp8", 2, 8192, 8192, 8192, "kn",
+                    ("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"),
+                    a_std=1 / math.sqrt(8192), b_std=1 / math.sqrt(8192), bias_std=0.1,
+                    alpha=0.5, fp8_scale=448.0 / 4.0),
+    "downproj": Workload("downproj", 3, 16384, 4096, 14336, "kn",
+                         ("residual", "store_bf16", "row_rms:1e-6"),
+                         a_std=1 / math.sqrt(14336), b_std=0.02, aux="residual"),
+    "backward": Workload("backward", 4, 8192, 16384, 4096, "nk",
+                         ("gelu_tanh_grad", "store_bf16", "col_sum"),
+                         a_std=1.0, b_std=0.02, aux="preact"),
+}
+
+BY_INDEX = {w.index: w for w in WORKLOADS.values()}
+
+
+@dataclass
+class Inputs:
+    A: torch.Tensor                 # M x K bf16
+    B: torch.Tensor                 # K x N or N x K bf16
+    bias: Optional[torch.Tensor]    # fp32, length = columns where the bias op sits
+    aux: Optional[torch.Tensor]     # M x n_out bf16 (residual or preact)
+    alpha: float
+    fp8_scale: float
+    extra: dict = field(default_factory=dict)
+
+
+def _bias_len(w: Workload) -> int:
+    prog = list(w.program)
+    if "bias" not in prog:
+        return 0
+    ib = prog.index("bias")
+    ip = next((i for i, op in enumerate(prog) if op.startswith("pair_swiglu")), None)
+    return w.N if (ip is None or ib < ip) else w.N // 2
+
+
+def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs:
+    """Draws the workload's tensors with a generator on ``device``."""
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + w.index if seed is None else seed)
+
+    def draw(shape, std, dtype=torch.bfloat16):
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        t.mul_(std)
+        return t.to(dtype)
+
+    A = draw((w.M, w.K), w.a_std)
+    B = draw((w.K, w.N) if w.b_layout == "kn" else (w.N, w.K), w.b_std)
+    nb = _bias_len(w)
+    bias = draw((nb,), w.bias_std, torch.float32) if nb else None
+    aux = draw((w.M, w.n_out), w.aux_std) if w.aux else None
+    return Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale)
+
+
+def bf16_bits(t: torch.Tensor):
+    """Host numpy uint16 view of a bf16 tensor's bit patterns."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")

@@ -1,0 +1,59 @@
+/*
+ * oracle.h -- fp64 CPU reference of the fused GEMM + epilogue.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py.  Shares nothing with the CUDA
+ * library.  See oracle.c for the definition and its sources.
+ */
+#ifndef GEMM_EPI_ORACLE_H
+#define GEMM_EPI_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int64_t M, N, K;
+    int b_is_nk;                 /* 0: B is K x N row-major; 1: B is N x K row-major */
+    const uint16_t *A;           /* bf16 bit patterns, M x K, row stride lda */
+    int64_t lda;
+    const uint16_t *B;           /* bf16 bit patterns */
+    int64_t ldb;
+    double alpha;                /* op "alpha" */
+    const float *bias;           /* op "bias": one value per column at its point of use */
+    const float *row_scale;      /* op "row_scale": M values */
+    const uint16_t *residual;    /* op "residual": bf16, M x (columns), row stride ld_aux */
+    const uint16_t *preact;      /* op "gelu_tanh_grad": bf16, same shape and stride */
+    int64_t ld_aux;
+    double fp8_scale;            /* op "store_e4m3": code = e4m3(value * fp8_scale) */
+    const char *program;         /* comma-separated op names, optional ":arg" */
+} oracle_problem;
+
+/* Whole output rows for the listed row indices (rows == NULL: rows 0..nrows-1).
+ * Every output pointer may be NULL.  y: value at store_bf16 (or final value),
+ * nrows x out_cols.  Returns 0, -1 for a bad program, -2 for a bad index. */
+int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
+                double *y, uint16_t *c_bf16, uint8_t *c_e4m3, double *row_stat,
+                double *amax_rows);
+
+/* Whole output columns (all M rows) for the listed columns.  y: M x ncols. */
+int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
+                double *y, double *col_stat);
+
+int oracle_out_cols(const oracle_problem *p);
+
+double oracle_bf16_to_double(uint16_t bits);
+uint16_t oracle_double_to_bf16(double x);
+uint8_t oracle_double_to_e4m3(double x);
+double oracle_e4m3_to_double(uint8_t c);
+double oracle_gelu_tanh(double x);
+double oracle_gelu_tanh_grad(double x);
+double oracle_silu(double x);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

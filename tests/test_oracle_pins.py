@@ -1,0 +1,374 @@
+"""Pins of the fp64 CPU oracle to things other than itself.
+
+Each test checks the oracle against numpy, a closed form, an exact special
+case, a hand-derived table or a pure-Python brute force, chosen so that a
+plausible mistake (a dropped term, a wrong sign or index, a transposed
+operand, swapped gate/up) fails at least one of them.  CPU only.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import Problem
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+RNG = np.random.default_rng(7)
+
+
+def bf16_bits_from_f32(x):
+    """bf16 bit patterns via torch's own float32 -> bfloat16 conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def rand_bf16(shape, scale=1.0):
+    return bf16_bits_from_f32(RNG.standard_normal(shape) * scale)
+
+
+def f64(bits):
+    return oracle.bf16_bits_to_f64(bits)
+
+
+# ---------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (17, 33, 65), (64, 40, 24)])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_gemm_matches_numpy_einsum(M, N, K, layout):
+    A = rand_bf16((M, K))
+    B = rand_bf16((K, N) if layout == "kn" else (N, K))
+    y = Problem(A, B, [], b_is_nk=(layout == "nk")).rows()["y"]
+    Bk = f64(B) if layout == "kn" else f64(B).T
+    ref = np.einsum("mk,kn->mn", f64(A), Bk)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_integer_exact():
+    A = bf16_bits_from_f32(RNG.integers(-2, 3, (24, 40)))
+    B = bf16_bits_from_f32(RNG.integers(-2, 3, (40, 16)))
+    y = Problem(A, B, []).rows()["y"]
+    ref = f64(A).astype(np.int64) @ f64(B).astype(np.int64)
+    assert np.array_equal(y, ref.astype(np.float64))
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_identity_and_permutation(layout):
+    K = 12
+    B = rand_bf16((K, 9) if layout == "kn" else (9, K))
+    Bkn = f64(B) if layout == "kn" else f64(B).T
+    eye = bf16_bits_from_f32(np.eye(K))
+    y = Problem(eye, B, [], b_is_nk=(layout == "nk")).rows()["y"]
+    assert np.array_equal(y, Bkn)
+    perm = RNG.permutation(K)
+    P = bf16_bits_from_f32(np.eye(K)[perm])
+    y = Problem(P, B, [], b_is_nk=(layout == "nk")).rows()["y"]
+    assert np.array_equal(y, Bkn[perm])
+
+
+def test_gemm_transposed_operand_is_caught():
+    """Planted mistake: reading a K x N B as if it were N x K must not pass
+    the einsum pin (square, non-symmetric B)."""
+    A = rand_bf16((4, 8))
+    B = rand_bf16((8, 8))
+    wrong = Problem(A, B, [], b_is_nk=True).rows()["y"]
+    ref = f64(A) @ f64(B)
+    assert not np.allclose(wrong, ref, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- activations
+
+def gelu_tanh_textbook(x):
+    return 0.5 * x * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+@pytest.mark.parametrize("x", [-8.0, -3.0, -1.0, -0.75, -0.1, 0.0, 1e-3, 0.5, 1.0, 2.5, 6.0])
+def test_gelu_tanh_closed_forms(x):
+    g = oracle.gelu_tanh
+    assert g(x) == pytest.approx(gelu_tanh_textbook(x), rel=1e-12, abs=1e-15)
+    assert g(x) - g(-x) == pytest.approx(x, rel=1e-12, abs=1e-15)
+    d = oracle.gelu_tanh_grad
+    assert d(x) + d(-x) == pytest.approx(1.0, rel=1e-12)
+    h = 1e-5
+    fd = (gelu_tanh_textbook(x + h) - gelu_tanh_textbook(x - h)) / (2 * h)
+    assert d(x) == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+def test_gelu_special_values():
+    assert oracle.gelu_tanh(0.0) == 0.0
+    assert oracle.gelu_tanh_grad(0.0) == 0.5
+
+
+@pytest.mark.parametrize("x", [-30.0, -4.0, -1.0, 0.0, 0.25, 1.0, 4.0, 30.0])
+def test_silu_closed_forms(x):
+    s = oracle.silu
+    assert s(x) == pytest.approx(x / (1.0 + math.exp(-x)), rel=1e-14, abs=1e-300)
+    assert s(x) - s(-x) == pytest.approx(x, rel=1e-12, abs=1e-15)
+    assert oracle.silu(0.0) == 0.0
+
+
+# ---------------------------------------------------------------- number formats
+
+def test_bf16_matches_torch_rounding():
+    x = np.concatenate([RNG.standard_normal(4000) * 10.0 ** RNG.integers(-30, 30, 4000),
+                        [1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130, 3e38]])
+    x32 = x.astype(np.float32)
+    ours = oracle.to_bf16_bits(x32.astype(np.float64))
+    theirs = bf16_bits_from_f32(x32)
+    assert np.array_equal(ours, theirs)
+
+
+def test_bf16_ties_to_even():
+    assert oracle.bf16_bits_to_f64(oracle.to_bf16_bits([1 + 2 ** -8]))[0] == 1.0
+    assert oracle.bf16_bits_to_f64(oracle.to_bf16_bits([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+
+
+def _golden_e4m3():
+    rows = []
+    with open(os.path.join(HERE, "golden", "e4m3_codes.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tok = line.split()
+            v = tok[0]
+            if "2^" in v:
+                coef, _, exp = v.partition("2^")
+                coef = coef.rstrip("*")
+                neg = coef.startswith("-")
+                coef = coef.lstrip("-")
+                val = (float(coef) if coef else 1.0) * 2.0 ** int(exp)
+                val = -val if neg else val
+            else:
+                val = float(v)
+            rows.append((val, int(tok[1], 16)))
+    return rows
+
+
+@pytest.mark.parametrize("value,code", _golden_e4m3())
+def test_e4m3_golden_codes(value, code):
+    assert int(oracle.to_e4m3([value])[0]) == code
+
+
+def test_e4m3_matches_torch_in_range():
+    x = np.concatenate([RNG.uniform(-448, 448, 3000), RNG.standard_normal(3000) * 0.01])
+    ours = oracle.to_e4m3(x)
+    theirs = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # x is exactly representable in fp32 except for rounding of the draw itself;
+    # compare on the fp32 values both sides see.
+    ours32 = oracle.to_e4m3(x.astype(np.float32).astype(np.float64))
+    assert np.array_equal(ours32, theirs)
+    assert ours.shape == theirs.shape
+
+
+def test_e4m3_decode_encode_round_trip():
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            assert math.isnan(oracle.e4m3_to_f64([c])[0])
+            continue
+        v = oracle.e4m3_to_f64([c])[0]
+        assert int(oracle.to_e4m3([v])[0]) == c
+
+
+# ---------------------------------------------------------------- epilogue ops
+
+def brute_force(A, B, b_is_nk, program, alpha=1.0, bias=None, row_scale=None, aux=None,
+                fp8_scale=1.0):
+    """Pure-Python loops (independent of oracle.c) for tiny problems, with the
+    tanh textbook form of GELU and a finite-difference-free GELU derivative
+    written as d/dx of 0.5 x (1 + tanh(u))."""
+    Af, Bf = f64(A), f64(B)
+    M, K = Af.shape
+    N = Bf.shape[0] if b_is_nk else Bf.shape[1]
+
+    def acc(m, n):
+        s = 0.0
+        for k in range(K):
+            s += Af[m, k] * (Bf[n, k] if b_is_nk else Bf[k, n])
+        return s
+
+    def gelu_grad(x):
+        c = math.sqrt(2 / math.pi)
+        u = c * (x + 0.044715 * x ** 3)
+        t = math.tanh(u)
+        return 0.5 * (1 + t) + 0.5 * x * (1 - t * t) * c * (1 + 3 * 0.044715 * x * x)
+
+    def silu(x):
+        return x / (1 + math.exp(-x))
+
+    def ew(op, y, m, n):
+        if op == "alpha":
+            return alpha * y
+        if op == "bias":
+            return y + float(bias[n])
+        if op == "row_scale":
+            return y * float(row_scale[m])
+        if op == "residual":
+            return y + f64(aux)[m, n]
+        if op == "gelu_tanh":
+            return gelu_tanh_textbook(y)
+        if op == "relu":
+            return max(y, 0.0)
+        if op == "silu":
+            return silu(y)
+        if op == "gelu_tanh_grad":
+            return y * gelu_grad(f64(aux)[m, n])
+        raise KeyError(op)
+
+    pair = [i for i, op in enumerate(program) if op.startswith("pair_swiglu")]
+    nout = N // 2 if pair else N
+    out = {"y": np.zeros((M, nout)), "amax": 0.0, "col": np.zeros(nout), "row": np.zeros(M)}
+    for m in range(M):
+        for j in range(nout):
+            if pair:
+                ip = pair[0]
+                g = int(program[ip].split(":")[1]) if ":" in program[ip] else 1
+                cg = (j // g) * 2 * g + j % g
+                cu = cg + g
+                yg, yu = acc(m, cg), acc(m, cu)
+                for op in program[:ip]:
+                    yg, yu = ew(op, yg, m, cg), ew(op, yu, m, cu)
+                y = silu(yg) * yu
+                rest = program[ip + 1:]
+            else:
+                y = acc(m, j)
+                rest = program
+            stored = None
+            for op in rest:
+                if op == "store_bf16":
+                    stored = y
+                elif op == "amax":
+                    out["amax"] = max(out["amax"], abs(y))
+                elif op == "col_sum":
+                    out["col"][j] += y
+                elif op.startswith("row_rms"):
+                    out["row"][m] += f64(bf16_bits_from_f32(np.array([y])))[0] ** 2
+                elif op == "store_e4m3":
+                    pass
+                else:
+                    y = ew(op, y, m, j)
+            out["y"][m, j] = y if stored is None else stored
+    return out
+
+
+PROGRAMS = [
+    (("alpha", "bias", "gelu_tanh", "amax", "store_bf16"), "kn"),
+    (("pair_swiglu", "store_bf16"), "kn"),
+    (("pair_swiglu:4", "store_bf16"), "kn"),
+    (("alpha", "bias", "pair_swiglu", "store_bf16"), "kn"),
+    (("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"), "kn"),
+    (("residual", "store_bf16", "row_rms:1e-6"), "kn"),
+    (("gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
+    (("row_scale", "silu", "store_bf16"), "nk"),
+]
+
+
+@pytest.mark.parametrize("program,layout", PROGRAMS)
+def test_oracle_matches_brute_force(program, layout):
+    M, N, K = 5, 16, 9
+    A = rand_bf16((M, K), 0.7)
+    B = rand_bf16((K, N) if layout == "kn" else (N, K), 0.7)
+    pair = any(op.startswith("pair") for op in program)
+    nout = N // 2 if pair else N
+    bias = None
+    if "bias" in program:
+        ip = next((i for i, op in enumerate(program) if op.startswith("pair")), None)
+        bias_len = N if (ip is not None and program.index("bias") < ip) else nout
+        bias = RNG.standard_normal(bias_len).astype(np.float32) * 0.1
+    row_scale = RNG.uniform(0.5, 2.0, M).astype(np.float32)
+    aux = rand_bf16((M, nout))
+    uses_aux = "residual" in program or "gelu_tanh_grad" in program
+    p = Problem(A, B, list(program), b_is_nk=(layout == "nk"), alpha=0.75, bias=bias,
+                row_scale=row_scale, residual=aux if "residual" in program else None,
+                preact=aux if "gelu_tanh_grad" in program else None, fp8_scale=112.0)
+    got = p.rows()
+    ref = brute_force(A, B, layout == "nk", list(program), alpha=0.75, bias=bias,
+                      row_scale=row_scale, aux=aux if uses_aux else None)
+    np.testing.assert_allclose(got["y"], ref["y"], rtol=1e-12, atol=1e-14)
+    if "amax" in program:
+        assert got["amax"] == pytest.approx(ref["amax"], rel=1e-12)
+    if "col_sum" in program:
+        cs = p.cols(list(range(nout)))
+        np.testing.assert_allclose(cs["col_stat"], ref["col"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(cs["y"], got["y"], rtol=1e-15, atol=0)
+    if any(op.startswith("row_rms") for op in program):
+        want = 1.0 / np.sqrt(ref["row"] / nout + 1e-6)
+        np.testing.assert_allclose(got["row_stat"], want, rtol=1e-12)
+
+
+def test_swapped_gate_up_is_caught():
+    """Planted mistake: swapping gate and up (up * silu(gate) vs gate *
+    silu(up)) must differ from the brute force."""
+    A = rand_bf16((3, 6))
+    B = rand_bf16((6, 8))
+    good = brute_force(A, B, False, ["pair_swiglu", "store_bf16"])["y"]
+    # Build the swapped version through the oracle by exchanging B's columns.
+    Bs = B.copy()
+    Bs[:, 0::2], Bs[:, 1::2] = B[:, 1::2], B[:, 0::2]
+    swapped = Problem(A, Bs, ["pair_swiglu", "store_bf16"]).rows()["y"]
+    assert not np.allclose(good, swapped, rtol=1e-6)
+
+
+def test_swiglu_identity_pin():
+    """A = I: out[m, j] = silu(B[m, 2j]) * B[m, 2j+1], values known exactly."""
+    K = 8
+    B = rand_bf16((K, 12))
+    y = Problem(bf16_bits_from_f32(np.eye(K)), B, ["pair_swiglu", "store_bf16"]).rows()["y"]
+    Bf = f64(B)
+    want = Bf[:, 0::2] / (1 + np.exp(-Bf[:, 0::2])) * Bf[:, 1::2]
+    np.testing.assert_allclose(y, want, rtol=1e-14)
+
+
+def test_row_scale_rewrite_identity():
+    """(X*S)@W == (X@W)*S for a row-broadcast S (powers of two keep X*S exact)."""
+    M, K, N = 6, 10, 7
+    X = rand_bf16((M, K))
+    W = rand_bf16((K, N))
+    S = (2.0 ** RNG.integers(-3, 4, M)).astype(np.float32)
+    XS = bf16_bits_from_f32(f64(X) * S[:, None])
+    lhs = Problem(XS, W, ["store_bf16"]).rows()["y"]
+    rhs = Problem(X, W, ["row_scale", "store_bf16"], row_scale=S).rows()["y"]
+    assert np.array_equal(lhs, rhs)
+
+
+def test_row_rms_constant_rows_closed_form():
+    M, K, N = 4, 8, 16
+    A = np.zeros((M, K), np.uint16)
+    B = rand_bf16((K, N))
+    c = np.array([0.5, -2.0, 3.0, 0.0])
+    res = bf16_bits_from_f32(np.repeat(c[:, None], N, 1))
+    r = Problem(A, B, ["residual", "store_bf16", "row_rms:1e-6"], residual=res).rows()["row_stat"]
+    np.testing.assert_allclose(r, 1 / np.sqrt(c * c + 1e-6), rtol=1e-15)
+
+
+def test_amax_and_stores_consistent():
+    A = rand_bf16((20, 32))
+    B = rand_bf16((32, 24))
+    bias = RNG.standard_normal(24).astype(np.float32)
+    out = Problem(A, B, ["alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"],
+                  alpha=0.5, bias=bias, fp8_scale=112.0).rows()
+    assert out["amax"] == np.abs(out["y"]).max()
+    assert np.all(out["y"] >= 0)
+    assert np.array_equal(out["c_bf16"], oracle.to_bf16_bits(out["y"]))
+    assert np.array_equal(out["c_e4m3"], oracle.to_e4m3(out["y"] * 112.0))
+    # bf16(amax) equals the max of the stored bf16 values (rounding is monotone).
+    assert oracle.to_bf16_bits([out["amax"]])[0] == out["c_bf16"].max()
+
+
+def test_cols_match_rows():
+    A = rand_bf16((9, 16))
+    W = rand_bf16((12, 16))
+    pre = rand_bf16((9, 12))
+    p = Problem(A, W, ["gelu_tanh_grad", "store_bf16", "col_sum"], b_is_nk=True, preact=pre)
+    rows = p.rows()["y"]
+    cols = p.cols([0, 3, 11])
+    np.testing.assert_array_equal(cols["y"], rows[:, [0, 3, 11]])
+    np.testing.assert_allclose(cols["col_stat"], rows[:, [0, 3, 11]].sum(0), rtol=1e-13)
+
+
+def test_bad_program_rejected():
+    A = rand_bf16((2, 2))
+    with pytest.raises(ValueError):
+        Problem(A, A, ["no_such_op"]).rows()
