@@ -1,0 +1,437 @@
+"""Benchmark of the fused GEMM + epilogue engine on GB300.
+
+One step = one pass of the whole hot path (TMA-fed tcgen05 main loop plus the
+on-chip epilogue program) over one batch of the synthetic workload, with its
+inputs resident in HBM.  The default workload is the MLP up-projection with
+the interleaved SwiGLU epilogue (A 8192x4096, B 4096x28672 -> 8192x14336).
+
+Prints ONE JSON line (rank 0).  Metric: fused GEMM+epilogue TFLOP/s
+(2*M*N*K per step), with the roofline fraction, the bare-GEMM time (same main
+loop, store-only epilogue) and the resulting epilogue overhead, an unfused
+two-pass time, an end-to-end number through the C ABI from pinned host
+buffers, and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 BF16 roofline; overhead vs bare GEMM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_NAME = "fused_gemm_epilogue_kernel"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="swiglu")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip bare / unfused comparison runs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gemm_epilogue_transformer_smem_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source (else None)."""
+    cur = kernel_source_hash()
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(f).read()
+        m = re.search(r"bench-traffic:\s*workload=(\S+)\s+source=(\S+)\s+bytes_per_launch=(\d+)", text)
+        if m and m.group(1) == workload and m.group(2) == cur:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= (self.t1 or 1e18) + 0.05]
+        use = inside or rows[-3:]
+        sm = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in use:
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max((float(p[3]) for _, p in use
+                                    if re.match(r"^[0-9.]+$", p[3])), default=None)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (x itself at world size 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_rows_sample(w, inp, seconds: float):
+    """Times the CPU oracle on leading rows of the workload, growing the row
+    count until about `seconds` of work.  Returns (tflops, rows, threads)."""
+    import oracle
+    from gemm_epilogue_transformer_smem_gb300 import synth
+
+    A = synth.bf16_bits(inp.A)
+    B = synth.bf16_bits(inp.B)
+    aux = synth.bf16_bits(inp.aux) if inp.aux is not None else None
+    prob = oracle.Problem(A, B, list(w.program), b_is_nk=(w.b_layout == "nk"), alpha=inp.alpha,
+                          bias=None if inp.bias is None else inp.bias.cpu().numpy(),
+                          residual=aux if w.aux == "residual" else None,
+                          preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale)
+    threads = oracle.cpu_threads()
+    rows = max(1, min(w.M, threads))
+    while True:
+        t0 = time.perf_counter()
+        prob.rows(list(range(rows)))
+        dt = time.perf_counter() - t0
+        if dt >= seconds * 0.5 or rows >= w.M:
+            break
+        rows = min(w.M, max(rows + 1, int(rows * min(8.0, seconds / max(dt, 1e-3)))))
+    flops = 2.0 * rows * w.N * w.K
+    return flops / dt / 1e12, rows, threads, dt
+
+
+def host_inputs(w, seed=None):
+    from gemm_epilogue_transformer_smem_gb300 import synth
+    return synth.make_inputs(w, "cpu", seed=seed)
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on bounded samples."""
+    from gemm_epilogue_transformer_smem_gb300 import synth
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    inp = host_inputs(w)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # size one step once, then run warmup + steps of that size
+    _, rows, threads, _ = oracle_rows_sample(w, inp, per_step)
+    import oracle
+    prob = oracle.Problem(synth.bf16_bits(inp.A), synth.bf16_bits(inp.B), list(w.program),
+                          b_is_nk=(w.b_layout == "nk"), alpha=inp.alpha,
+                          bias=None if inp.bias is None else inp.bias.numpy(),
+                          residual=synth.bf16_bits(inp.aux) if w.aux == "residual" else None,
+                          preact=synth.bf16_bits(inp.aux) if w.aux == "preact" else None,
+                          fp8_scale=inp.fp8_scale)
+    for _ in range(args.warmup):
+        prob.rows(list(range(rows)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        prob.rows(list(range(rows)))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = "%d of %d rows (all %d columns, K=%d) per step" % (rows, w.M, w.n_out, w.K)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "program": list(w.program)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_steps(fn, steps, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from gemm_epilogue_transformer_smem_gb300 import api, build, synth
+
+    build.build()
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w, dev)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout)
+    out = api.allocate_outputs(plan, dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux)
+
+    def step():
+        api.run_program(plan, inp.A, inp.B, out, **kw)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = plan.query_status(out.workspace)
+    if status != 0:
+        raise RuntimeError("fused kernel reported status %d" % status)
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("begin")
+    seconds = time_steps(step, args.steps, stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    barrier(world)
+    seconds = max_over_ranks(seconds, world)
+    clk = clocks.stop() if rank == 0 else None
+    flops = float(w.flops)
+    value = aggregate_value(flops * args.steps, world, seconds) / 1e12
+    ms_per_step = seconds / args.steps * 1e3
+    fused_tflops = flops / (seconds / args.steps) / 1e12
+
+    extras = {}
+    if not args.no_extras:
+        k2 = max(5, min(args.steps, 100))
+        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout)
+        bare_out = api.allocate_outputs(bare, dev)
+
+        def bare_step():
+            bare.run(inp.A, inp.B, C=bare_out.C, workspace=bare_out.workspace)
+
+        for _ in range(3):
+            bare_step()
+        t_bare = time_steps(bare_step, k2, stream) / k2
+        scratch = bare_out.C
+
+        def unfused_step():
+            api.run_program(plan, inp.A, inp.B, out, unfused_scratch=scratch, **kw)
+
+        for _ in range(3):
+            unfused_step()
+        t_unf = time_steps(unfused_step, k2, stream) / k2
+        t_fused = time_steps(step, k2, stream) / k2
+        extras = {
+            "bare_gemm_ms": t_bare * 1e3, "bare_gemm_tflops": flops / t_bare / 1e12,
+            "unfused_ms": t_unf * 1e3, "unfused_tflops": flops / t_unf / 1e12,
+            "fused_ms_same_window": t_fused * 1e3,
+            "overhead_vs_bare": t_fused / t_bare - 1.0,
+        }
+        del bare_out, scratch
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(plan, w, inp, out, kw, dev, max(3, min(args.steps, 20)), world)
+
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": fused_tflops / peak, "traffic": traffic,
+                "peak_source": "%s burst bf16 (cuBLAS)" % src,
+                "algorithmic_flops_per_launch": flops}
+    cpu = None
+    if not args.no_cpu:
+        host = synth.make_inputs(w, "cpu")
+        tf, rows, threads, dt = oracle_rows_sample(w, host, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d rows x all %d output columns, K=%d (%.1f s)" % (
+                   rows, w.M, w.n_out, w.K, dt)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "b_layout": w.b_layout,
+                   "program": list(w.program), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: inputs + output (%d MB) exceed the 129 MB L2" % (
+                       (inp.A.numel() + inp.B.numel()) * 2 // 2 ** 20 + plan.M * plan.n_out * 2 // 2 ** 20)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        **extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
+    """Same metric through the C ABI with host buffers: every step copies the
+    inputs from pinned host memory, runs, and reads the outputs back."""
+    import torch
+    from gemm_epilogue_transformer_smem_gb300 import api
+
+    h = {k: (v.cpu().pin_memory() if v is not None else None)
+         for k, v in (("A", inp.A), ("B", inp.B), ("bias", inp.bias), ("aux", inp.aux))}
+    d = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
+    outs = [t for t in (out.C, out.C8, out.amax, out.row_out, out.col_out) if t is not None]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k, v in h.items():
+            if v is not None:
+                d[k].copy_(v, non_blocking=True)
+        api.run_program(plan, d["A"], d["B"], out, alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
+                        bias=d["bias"], aux=d["aux"])
+        for t, ht in zip(outs, host_out):
+            ht.copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    seconds = time_steps(step, steps, stream)
+    seconds = max_over_ranks(seconds, world)
+    value = aggregate_value(float(w.flops) * steps, world, seconds) / 1e12
+    return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": seconds / steps * 1e3}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

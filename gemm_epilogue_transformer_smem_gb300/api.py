@@ -1,0 +1,173 @@
+"""Torch-facing wrapper over the C ABI: builds the descriptor from an op list,
+passes tensor data pointers and the current CUDA stream.  No arithmetic of the
+method happens here; every step runs in the CUDA library.
+
+Programs are written as op names (one optional numeric argument after a
+colon):
+
+  alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g],
+  gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
+  row_rms_unrounded[:eps], col_sum
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import native as N
+
+PROGRAM_OPS = {
+    "alpha": N.GEMM_EPI_OP_SCALE_ALPHA,
+    "bias": N.GEMM_EPI_OP_ADD_BIAS_COL,
+    "row_scale": N.GEMM_EPI_OP_MUL_ROW_SCALE,
+    "residual": N.GEMM_EPI_OP_ADD_RESIDUAL,
+    "gelu_tanh": N.GEMM_EPI_OP_ACT_GELU_TANH,
+    "relu": N.GEMM_EPI_OP_ACT_RELU,
+    "silu": N.GEMM_EPI_OP_ACT_SILU,
+    "pair_swiglu": N.GEMM_EPI_OP_PAIR_SWIGLU,
+    "gelu_tanh_grad": N.GEMM_EPI_OP_MUL_GELU_TANH_GRAD,
+    "amax": N.GEMM_EPI_OP_AMAX,
+    "store_bf16": N.GEMM_EPI_OP_STORE_BF16,
+    "store_e4m3": N.GEMM_EPI_OP_STORE_E4M3,
+    "row_rms": N.GEMM_EPI_OP_ROW_RMS_RSQRT,
+    "row_rms_unrounded": N.GEMM_EPI_OP_ROW_RMS_RSQRT,
+    "col_sum": N.GEMM_EPI_OP_COL_SUM,
+}
+
+
+def encode_program(program: Sequence[str]):
+    ops = (N.gemm_epi_op * max(1, len(program)))()
+    for i, spec in enumerate(program):
+        name, _, arg = spec.partition(":")
+        if name not in PROGRAM_OPS:
+            raise ValueError("unknown epilogue op %r" % name)
+        code = PROGRAM_OPS[name]
+        i0, f0 = 0, 0.0
+        if name == "pair_swiglu":
+            i0 = int(arg) if arg else 1
+        elif name.startswith("row_rms"):
+            f0 = float(arg) if arg else 1e-6
+            i0 = 1 if name == "row_rms_unrounded" else 0
+        ops[i] = N.gemm_epi_op(code, i0, f0)
+    return ops
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Plan:
+    """One validated GEMM + epilogue plan (gemm_epi_create).  Strides default
+    to tight row-major packing."""
+
+    def __init__(self, M: int, N_: int, K: int, program: Sequence[str], b_layout: str = "kn",
+                 lda: Optional[int] = None, ldb: Optional[int] = None, ldc: Optional[int] = None,
+                 ldc8: Optional[int] = None, ld_aux: Optional[int] = None):
+        self.lib = N.load()
+        self.program = list(program)
+        self.M, self.N, self.K = M, N_, K
+        self.b_layout = b_layout
+        pair = any(op.startswith("pair_swiglu") for op in program)
+        n_out = N_ // 2 if pair else N_
+        self._ops = encode_program(program)
+        d = N.gemm_epi_desc()
+        d.M, d.N, d.K = M, N_, K
+        d.lda = K if lda is None else lda
+        d.ldb = (N_ if b_layout == "kn" else K) if ldb is None else ldb
+        d.ldc = n_out if ldc is None else ldc
+        d.ldc8 = n_out if ldc8 is None else ldc8
+        d.ld_aux = n_out if ld_aux is None else ld_aux
+        d.b_layout = N.GEMM_EPI_B_KN if b_layout == "kn" else N.GEMM_EPI_B_NK
+        d.n_ops = len(program)
+        d.ops = ctypes.cast(self._ops, ctypes.POINTER(N.gemm_epi_op))
+        self.desc = d
+        h = N.gemm_epi_handle()
+        N.check(self.lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)), self.lib)
+        self.handle = h
+        self.n_out = int(self.lib.gemm_epi_out_cols(h))
+        self.workspace_bytes = int(self.lib.gemm_epi_workspace_size(h))
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            self.lib.gemm_epi_destroy(h)
+            self.handle = None
+
+    def args(self, A, B, *, alpha=1.0, fp8_scale=1.0, bias=None, row_scale=None, residual=None,
+             preact=None, C=None, C8=None, amax=None, row_out=None, col_out=None, workspace=None,
+             timeout_ms=0, debug_flags=0) -> N.gemm_epi_args:
+        a = N.gemm_epi_args()
+        a.A, a.B = _ptr(A), _ptr(B)
+        a.alpha, a.fp8_scale = float(alpha), float(fp8_scale)
+        a.bias, a.row_scale = _ptr(bias), _ptr(row_scale)
+        a.residual, a.preact = _ptr(residual), _ptr(preact)
+        a.C, a.C8 = _ptr(C), _ptr(C8)
+        a.amax, a.row_out, a.col_out = _ptr(amax), _ptr(row_out), _ptr(col_out)
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        a.timeout_ms, a.debug_flags = int(timeout_ms), int(debug_flags)
+        return a
+
+    def run(self, *tensors, stream: Optional[torch.cuda.Stream] = None, **kw):
+        """gemm_epi_run on the current (or given) CUDA stream; asynchronous."""
+        a = self.args(*tensors, **kw)
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        N.check(self.lib.gemm_epi_run(self.handle, ctypes.byref(a), ctypes.c_void_p(s)), self.lib)
+
+    def run_unfused(self, *tensors, scratch: torch.Tensor, stream=None, **kw):
+        a = self.args(*tensors, **kw)
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        N.check(self.lib.gemm_epi_run_unfused(self.handle, ctypes.byref(a), ctypes.c_void_p(scratch.data_ptr()),
+                                              scratch.stride(0), ctypes.c_void_p(s)), self.lib)
+
+    def query_status(self, workspace: torch.Tensor, stream=None) -> int:
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        return int(self.lib.gemm_epi_query_status(self.handle, ctypes.c_void_p(workspace.data_ptr()),
+                                                  ctypes.c_void_p(s)))
+
+
+@dataclass
+class Outputs:
+    C: Optional[torch.Tensor] = None
+    C8: Optional[torch.Tensor] = None
+    amax: Optional[torch.Tensor] = None
+    row_out: Optional[torch.Tensor] = None
+    col_out: Optional[torch.Tensor] = None
+    workspace: Optional[torch.Tensor] = None
+
+
+def allocate_outputs(plan: Plan, device) -> Outputs:
+    """Device buffers for every output the program writes (torch allocates)."""
+    prog = [op.partition(":")[0] for op in plan.program]
+    o = Outputs()
+    if "store_bf16" in prog:
+        o.C = torch.empty((plan.M, plan.n_out), dtype=torch.bfloat16, device=device)
+    if "store_e4m3" in prog:
+        o.C8 = torch.empty((plan.M, plan.n_out), dtype=torch.uint8, device=device)
+    if "amax" in prog:
+        o.amax = torch.empty(1, dtype=torch.float32, device=device)
+    if any(p.startswith("row_rms") for p in prog):
+        o.row_out = torch.empty(plan.M, dtype=torch.float32, device=device)
+    if "col_sum" in prog:
+        o.col_out = torch.empty(plan.n_out, dtype=torch.float32, device=device)
+    o.workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=device)
+    return o
+
+
+def run_program(plan: Plan, A, B, out: Outputs, *, alpha=1.0, fp8_scale=1.0, bias=None,
+                row_scale=None, aux=None, unfused_scratch=None, **kw) -> Outputs:
+    """Runs the plan with the auxiliary tensor routed to residual or preact."""
+    prog = [op.partition(":")[0] for op in plan.program]
+    residual = aux if "residual" in prog else None
+    preact = aux if "gelu_tanh_grad" in prog else None
+    tensors = dict(alpha=alpha, fp8_scale=fp8_scale, bias=bias, row_scale=row_scale,
+                   residual=residual, preact=preact, C=out.C, C8=out.C8, amax=out.amax,
+                   row_out=out.row_out, col_out=out.col_out, workspace=out.workspace, **kw)
+    if unfused_scratch is not None:
+        plan.run_unfused(A, B, scratch=unfused_scratch, **tensors)
+    else:
+        plan.run(A, B, **tensors)
+    return out

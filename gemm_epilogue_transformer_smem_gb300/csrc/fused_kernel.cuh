@@ -1,0 +1,723 @@
+// fused_kernel.cuh -- persistent tcgen05 GEMM with the epilogue program
+// finished on chip.
+//
+// What it computes: acc = A @ B on 128 x 256 output tiles ("Lean4-TileLang
+// Tensor Program Superoptimizer", section 8 "Matmul": tiles staged through
+// shared memory, a pipelined K loop, swizzled tile order, tensor cores), then
+// the epilogue primitives of include/gemm_epi.h on each tile while it is still
+// on chip ("CODA: ... GEMM-Epilogue", "How CODA works"; the TileLang
+// tutorial's fused bias + GELU epilogue; the cuDNN Graph API tutorial's
+// alpha / bias / activation / AMAX epilogue).
+//
+// How, on sm_103a:
+//   warp 0      TMA producer: A (K-major, 128x64 box) and B (K-major 256x64
+//               box, or four MN-major 64x64 boxes) into a STAGES-deep ring of
+//               128B-swizzled shared-memory stages, mbarrier transaction counts.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators),
+//               then one lane issues tcgen05.mma (M=128, N=256, K=16) and
+//               commits each stage back to the producer and each finished
+//               accumulator to the epilogue.
+//   warps 2..5  epilogue: warp w drains TMEM lanes 32*(w%4).. with
+//               tcgen05.ld (thread = row, register = column), runs the op
+//               program in registers, stages bf16 / e4m3 results in swizzled
+//               shared memory and writes them with TMA stores.  Residual and
+//               pre-activation tiles arrive by TMA two chunks ahead.
+// The accumulator is double-buffered, so a tile's epilogue overlaps the next
+// tile's main loop.  Tiles are walked persistently (grid = number of SMs) in
+// groups of `group_m` M-tiles so that neighbouring CTAs share A and B in L2.
+//
+// Every mbarrier wait is bounded: when one runs out the CTA records a status
+// in the workspace, raises a shared abort flag that every other wait checks,
+// waits (bounded) for its own copies and MMAs in flight, frees TMEM and exits.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/gemm_epi.h"
+#include "ptx.cuh"
+
+namespace ge {
+
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_N = 256;
+constexpr int BLOCK_K = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int CHUNK = 32;     // output columns per epilogue step
+constexpr int EPI_BUFS = 3;   // bf16 / aux staging buffers per epilogue warp
+constexpr int E8_BUFS = 2;    // e4m3 staging buffers per epilogue warp
+constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;
+
+constexpr uint32_t A_STAGE_BYTES = BLOCK_M * BLOCK_K * 2;
+constexpr uint32_t B_STAGE_BYTES = BLOCK_N * BLOCK_K * 2;
+constexpr uint32_t B_MN_BOX_BYTES = 64 * BLOCK_K * 2;  // one 64-column MN-major box
+constexpr uint32_t EPI_BUF_BYTES = 32 * CHUNK * 2;     // 32 rows x 64 bytes
+constexpr uint32_t E8_BUF_BYTES = 32 * CHUNK;          // 32 rows x 32 bytes
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+constexpr uint32_t OFF_E8 = OFF_EPI + NUM_EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+constexpr uint32_t OFF_BAR = OFF_E8 + NUM_EPI_WARPS * E8_BUFS * E8_BUF_BYTES;
+constexpr uint32_t BAR_FULL = 0;
+constexpr uint32_t BAR_EMPTY = BAR_FULL + STAGES;
+constexpr uint32_t BAR_TFULL = BAR_EMPTY + STAGES;
+constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 2;
+constexpr uint32_t BAR_AUX = BAR_TEMPTY + 2;
+constexpr uint32_t BAR_DRAIN = BAR_AUX + NUM_EPI_WARPS * EPI_BUFS;
+constexpr uint32_t NUM_BARS = BAR_DRAIN + 1;
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // room to align the base to 1 KB
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
+static_assert(OFF_EPI % 1024 == 0 && OFF_E8 % 1024 == 0, "staging buffers must stay aligned");
+
+// Program flags derived on the host.
+enum : uint32_t {
+  F_AUX = 1u << 0,    // residual or preact tile is read
+  F_STORE = 1u << 1,  // bf16 C is written
+  F_E8 = 1u << 2,     // e4m3 C8 is written
+  F_AMAX = 1u << 3,
+  F_ROW = 1u << 4,
+  F_COL = 1u << 5,
+  F_ZERO_ACC = 1u << 6,  // K == 0: the accumulator is zero, TMEM is not read
+};
+
+// Where a bounded wait ran out (second status word).
+enum : uint32_t {
+  W_PRODUCER_EMPTY = 1,
+  W_MMA_FULL = 2,
+  W_MMA_TMEM_EMPTY = 3,
+  W_EPI_TMEM_FULL = 4,
+  W_EPI_AUX = 5,
+  W_DRAIN = 6,
+};
+
+struct EpiOpDev {
+  int32_t code;
+  int32_t i0;
+  float f0;
+};
+
+struct KernelParams {
+  int32_t M, N, K, n_out;
+  int32_t num_m_tiles, num_n_tiles, num_tiles, num_k_blocks;
+  int32_t group_m;
+  int32_t b_kn;  // 1: B stored K x N (MN-major operand)
+  uint32_t idesc;
+  uint32_t flags;
+  int32_t n_ops;
+  int32_t pair_at;  // index of PAIR_SWIGLU in ops, or -1
+  int32_t pair_g;
+  float alpha, fp8_scale, rms_eps;
+  int32_t rms_unrounded;
+  const float* bias;
+  const float* row_scale;
+  float* amax;
+  float* row_out;
+  float* col_out;
+  uint32_t* status;       // workspace: [0] error bits, [1] where, [2] block
+  uint32_t* row_counter;  // workspace: one arrival counter per M tile
+  uint64_t timeout_ns;
+  uint32_t debug_flags;
+  EpiOpDev ops[GEMM_EPI_MAX_OPS];
+};
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& mb, int& nb) {
+  const int per_group = p.group_m * p.num_n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * p.group_m;
+  const int gsz = min(p.num_m_tiles - first_m, p.group_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       const KernelParams& p, uint32_t where) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+#pragma unroll 1
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1u;
+      if (atomicOr(p.status, 1u) == 0u) {
+        p.status[1] = where;
+        p.status[2] = blockIdx.x;
+      }
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+// Bounded wait for the phase of parity `parity` of mbarrier `bar`.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         const KernelParams& p, uint32_t where) {
+  if (ptx::mbar_test(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, p, where);
+}
+
+// Short bounded wait used while draining after an abort (no flag check).
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+#pragma unroll 1
+  while (!ptx::mbar_test(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// tcgen05 shared-memory descriptor for a 128B-swizzled operand tile.
+// K-major: rows of 128 bytes along K, 8-row groups SBO = 1024 bytes apart.
+// MN-major: 64-element (128 B) rows along MN, 8 K-rows per 1024-byte group
+// (SBO), successive 64-element MN blocks LBO bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
+// ------------------------------------------------------------------ math
+
+constexpr float LOG2E = 1.4426950408889634f;
+// 2 * sqrt(2/pi) and that times 0.044715: 2u = x * (GELU_K0 + GELU_K1 x^2)
+constexpr float GELU_K0 = 1.5957691216057308f;
+constexpr float GELU_K1 = 1.5957691216057308f * 0.044715f;
+
+// 1 / (1 + e^-z) with e^-z = 2^(-z log2 e), the exp2 form the Superoptimizer
+// page uses for SiLU (section 7).
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return ptx::rcp_approx(1.0f + ptx::ex2_approx(-z * LOG2E));
+}
+
+// GELU, tanh approximation, as x * sigmoid(2u).
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  return x * sigmoid_f(x * fmaf(GELU_K1, x * x, GELU_K0));
+}
+
+// d/dx of x * sigmoid(2u) = s + x s (1 - s) (2u)'.
+__device__ __forceinline__ float gelu_tanh_grad_f(float x) {
+  const float x2 = x * x;
+  const float s = sigmoid_f(x * fmaf(GELU_K1, x2, GELU_K0));
+  return fmaf(x * s * (1.0f - s), fmaf(3.0f * GELU_K1, x2, GELU_K0), s);
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+
+__device__ __forceinline__ float bf16_round_f(float x) {
+  const uint32_t h = ptx::pack_bf16x2(x, 0.0f) & 0xFFFFu;
+  return __uint_as_float(h << 16);
+}
+
+// Element-wise ops that may run on accumulator columns (before the pair op)
+// or on output columns.  Columns of v[j]: col0 + j; `ncols` bounds the bias.
+template <int NV>
+__device__ __forceinline__ void apply_pointwise(const EpiOpDev& op, float (&v)[NV],
+                                                const KernelParams& p, int col0, int ncols,
+                                                float row_scale_m) {
+  switch (op.code) {
+    case GEMM_EPI_OP_SCALE_ALPHA:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] *= p.alpha;
+      break;
+    case GEMM_EPI_OP_ADD_BIAS_COL:
+      if (col0 + NV <= ncols) {
+        const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);
+#pragma unroll
+        for (int q = 0; q < NV / 4; ++q) {
+          const float4 b = __ldg(b4 + q);
+          v[4 * q + 0] += b.x;
+          v[4 * q + 1] += b.y;
+          v[4 * q + 2] += b.z;
+          v[4 * q + 3] += b.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < ncols) v[j] += __ldg(p.bias + col0 + j);
+      }
+      break;
+    case GEMM_EPI_OP_MUL_ROW_SCALE:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] *= row_scale_m;
+      break;
+    case GEMM_EPI_OP_ACT_GELU_TANH:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = gelu_tanh_f(v[j]);
+      break;
+    case GEMM_EPI_OP_ACT_RELU:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = fmaxf(v[j], 0.0f);
+      break;
+    case GEMM_EPI_OP_ACT_SILU:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = silu_f(v[j]);
+      break;
+    default:
+      break;
+  }
+}
+
+// out[j] = silu(a[gate(j)]) * a[up(j)] with gate(j) = (j/G)*2G + j%G, up = gate + G.
+template <int G>
+__device__ __forceinline__ void pair_swiglu_g(const float (&a)[64], float (&out)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int gate = (j / G) * 2 * G + (j % G);
+    out[j] = silu_f(a[gate]) * a[gate + G];
+  }
+}
+
+__device__ __forceinline__ void pair_swiglu(const float (&a)[64], float (&out)[32], int g) {
+  switch (g) {
+    case 2: pair_swiglu_g<2>(a, out); break;
+    case 4: pair_swiglu_g<4>(a, out); break;
+    case 8: pair_swiglu_g<8>(a, out); break;
+    case 16: pair_swiglu_g<16>(a, out); break;
+    case 32: pair_swiglu_g<32>(a, out); break;
+    default: pair_swiglu_g<1>(a, out); break;
+  }
+}
+
+// Lane l returns the sum over the warp's 32 lanes of x[l] (x is consumed).
+__device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? x[i] : x[i + s];
+      const float keep = upper ? x[i + s] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return x[0];
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fused_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tm_a,
+                               const __grid_constant__ CUtensorMap tm_b,
+                               const __grid_constant__ CUtensorMap tm_c,
+                               const __grid_constant__ CUtensorMap tm_c8,
+                               const __grid_constant__ CUtensorMap tm_aux,
+                               const __grid_constant__ KernelParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bar0 = sbase + OFF_BAR;
+  auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(BAR_FULL + s), 1);
+      ptx::mbar_init(bar(BAR_EMPTY + s), 1);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(BAR_TFULL + b), 1);
+      ptx::mbar_init(bar(BAR_TEMPTY + b), NUM_EPI_WARPS);
+    }
+    for (uint32_t i = 0; i < NUM_EPI_WARPS * EPI_BUFS; ++i) ptx::mbar_init(bar(BAR_AUX + i), 1);
+    ptx::mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + OFF_MISC, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_a);
+    ptx::tma_prefetch_desc(&tm_b);
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = misc[0];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0 && p.num_k_blocks > 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per-stage bits, for the abort drain
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_bar(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const bool skip = (p.debug_flags & GEMM_EPI_DEBUG_SKIP_FIRST_LOAD) && blockIdx.x == 0 &&
+                            t == static_cast<int>(blockIdx.x) && kb == 0;
+          if (!skip) {
+            const uint32_t fb = bar(BAR_FULL + stage);
+            ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+            const uint32_t sa = sbase + OFF_A + stage * A_STAGE_BYTES;
+            const uint32_t sb = sbase + OFF_B + stage * B_STAGE_BYTES;
+            ptx::tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, mb * BLOCK_M);
+            if (p.b_kn) {
+#pragma unroll
+              for (int j = 0; j < BLOCK_N / 64; ++j)
+                ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, &tm_b, fb, nb * BLOCK_N + j * 64,
+                                 kb * BLOCK_K);
+            } else {
+              ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, nb * BLOCK_N);
+            }
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          } else {
+            issued &= ~(1u << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (uint32_t s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, any_mma = false;
+      int local = 0;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+        const uint32_t buf = local & 1, use = local >> 1;
+        if (!wait_bar(bar(BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p, W_MMA_TMEM_EMPTY)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+        if (p.num_k_blocks == 0) {
+          ptx::mbar_arrive(bar(BAR_TFULL + buf));
+          continue;
+        }
+        const uint32_t d_tmem = tmem_base + buf * BLOCK_N;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_bar(bar(BAR_FULL + stage), phase, abort_flag, p, W_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t sa = sbase + OFF_A + stage * A_STAGE_BYTES;
+          const uint32_t sb = sbase + OFF_B + stage * B_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
+            const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
+            const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
+                                       : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
+            ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          any_mma = true;
+          ptx::mma_commit(bar(BAR_EMPTY + stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(BAR_TFULL + buf));
+      }
+      if (any_mma) {
+        // Every MMA this thread issued is complete before TMEM is released.
+        ptx::mma_commit(bar(BAR_DRAIN));
+        drain_wait(bar(BAR_DRAIN), 0, p.timeout_ns);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int ew = warp - 2;    // staging-buffer owner index 0..3
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may read
+    const int pair_at = p.pair_at;
+    const bool paired = pair_at >= 0;
+    const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
+    const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
+    const uint32_t flags = p.flags;
+    const uint32_t epi0 = sbase + OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
+    const uint32_t e80 = sbase + OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
+    uint8_t* epi0_ptr = smem + OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
+    uint8_t* e80_ptr = smem + OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
+    const int op_begin = paired ? pair_at + 1 : 0;
+    const uint64_t aux_policy = ptx::policy_evict_first();
+
+    uint32_t amax_bits = 0;
+    uint32_t gchunk = 0;                 // this warp's running chunk number
+    uint32_t aux_issued = 0, aux_done = 0;  // chunk numbers of aux loads
+    bool ok = true;
+    int local = 0;
+
+    auto issue_aux = [&](uint32_t g, int col, int row0) {
+      const uint32_t i = g % EPI_BUFS;
+      const uint32_t b = bar(BAR_AUX + ew * EPI_BUFS + i);
+      ptx::mbar_arrive_expect_tx(b, EPI_BUF_BYTES);
+      ptx::tma_load_2d_hint(epi0 + i * EPI_BUF_BYTES, &tm_aux, b, col, row0, aux_policy);
+    };
+
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int row_in_tile = quad * 32 + lane;
+      const int m = mb * BLOCK_M + row_in_tile;
+      const bool row_ok = m < p.M;
+      const int slab_row0 = mb * BLOCK_M + quad * 32;
+      const bool slab_ok = slab_row0 < p.M;
+      const int n0 = nb * tile_out_cols;       // first output column of the tile
+      const int nacc0 = nb * BLOCK_N;          // first accumulator column
+      const uint32_t buf = local & 1, use = local >> 1;
+      const float rs_m = (p.row_scale != nullptr && row_ok) ? __ldg(p.row_scale + m) : 0.0f;
+
+      if (flags & F_AUX) {
+        if (lane == 0) {
+          ptx::bulk_wait_group_read<0>();
+          const int first = min(2, chunks);
+          for (int c = 0; c < first; ++c) issue_aux(gchunk + c, n0 + c * CHUNK, slab_row0);
+          aux_issued = gchunk + first;
+        }
+        __syncwarp();
+      }
+
+      // All lanes wait; the outcome is made warp-uniform so that no lane
+      // leaves while the others enter a warp-synchronous step.
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(bar(BAR_TFULL + buf), use & 1u, abort_flag, p, W_EPI_TMEM_FULL))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BLOCK_N;
+      float row_ss = 0.0f;
+
+      for (int c = 0; c < chunks; ++c) {
+        const uint32_t g = gchunk + c;
+        const uint32_t eb = g % EPI_BUFS;
+        const int col0 = n0 + c * CHUNK;  // first output column of the chunk
+        float v[32];
+
+        // ---- accumulator -> registers (and the pair op)
+        if (!paired) {
+          if (flags & F_ZERO_ACC) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+          } else {
+            uint32_t r[32];
+            ptx::tmem_ld32_sync(t_row + c * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          }
+        } else {
+          float a[64];
+          if (flags & F_ZERO_ACC) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) a[j] = 0.0f;
+          } else {
+            uint32_t r[64];
+            ptx::tmem_ld64_sync(t_row + c * 64, r);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) a[j] = __uint_as_float(r[j]);
+          }
+          for (int i = 0; i < pair_at; ++i)
+            apply_pointwise<64>(p.ops[i], a, p, nacc0 + c * 64, p.N, rs_m);
+          pair_swiglu(a, v, p.pair_g);
+        }
+        if (c == chunks - 1) {
+          // The accumulator buffer is free for the next tile's MMAs.
+          ptx::tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(BAR_TEMPTY + buf));
+        }
+
+        // ---- auxiliary tile (residual / pre-activation), this thread's row
+        float x[32];
+        if (flags & F_AUX) {
+          if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_AUX + ew * EPI_BUFS + eb),
+                                                (g / EPI_BUFS) & 1u, abort_flag, p, W_EPI_AUX))) {
+            ok = false;
+            break;
+          }
+          aux_done = g + 1;
+          const uint8_t* rowp = epi0_ptr + eb * EPI_BUF_BYTES + lane * 64;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              x[8 * q + 2 * h] = __uint_as_float(ww[h] << 16);
+              x[8 * q + 2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = 0.0f;
+        }
+
+        // ---- the op program on output columns
+        const bool full_cols = col0 + 32 <= p.n_out;
+        for (int i = op_begin; i < p.n_ops; ++i) {
+          const EpiOpDev op = p.ops[i];
+          switch (op.code) {
+            case GEMM_EPI_OP_ADD_RESIDUAL:
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += x[j];
+              break;
+            case GEMM_EPI_OP_MUL_GELU_TANH_GRAD:
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
+              break;
+            case GEMM_EPI_OP_AMAX:
+              if (row_ok) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (full_cols || col0 + j < p.n_out)
+                    amax_bits = max(amax_bits, __float_as_uint(fabsf(v[j])));
+              }
+              break;
+            case GEMM_EPI_OP_STORE_BF16: {
+              uint8_t* rowp = epi0_ptr + eb * EPI_BUF_BYTES + lane * 64;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = ptx::pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+                w.y = ptx::pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+                w.z = ptx::pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+                w.w = ptx::pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+                *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
+              }
+              break;
+            }
+            case GEMM_EPI_OP_STORE_E4M3: {
+              uint8_t* rowp = e80_ptr + (g % E8_BUFS) * E8_BUF_BYTES + lane * 32;
+              const float s = p.fp8_scale;
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const int j = 16 * q + 4 * h;
+                  const uint32_t lo = ptx::pack_e4m3x2(v[j] * s, v[j + 1] * s);
+                  const uint32_t hi = ptx::pack_e4m3x2(v[j + 2] * s, v[j + 3] * s);
+                  w[h] = lo | (hi << 16);
+                }
+                *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 2) & 1)) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+              }
+              break;
+            }
+            case GEMM_EPI_OP_ROW_RMS_RSQRT:
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float u = p.rms_unrounded ? v[j] : bf16_round_f(v[j]);
+                if (full_cols || col0 + j < p.n_out) row_ss = fmaf(u, u, row_ss);
+              }
+              break;
+            case GEMM_EPI_OP_COL_SUM: {
+              float s[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) s[j] = row_ok ? v[j] : 0.0f;
+              const float tot = warp_transpose_sum(s, lane);
+              if (slab_ok && col0 + lane < p.n_out) atomicAdd(p.col_out + col0 + lane, tot);
+              break;
+            }
+            default:
+              apply_pointwise<32>(op, v, p, col0, p.n_out, rs_m);
+              break;
+          }
+        }
+
+        // ---- stores of this chunk, then the aux load two chunks ahead into
+        // the buffer whose store (chunk g-1) has finished reading it.
+        if (flags & (F_STORE | F_E8 | F_AUX)) {
+          ptx::fence_proxy_async_smem();  // generic smem accesses before async-proxy ones
+          __syncwarp();
+          if (lane == 0) {
+            if (flags & (F_STORE | F_E8)) {
+              if (slab_ok && col0 < p.n_out) {
+                if (flags & F_STORE)
+                  ptx::tma_store_2d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0);
+                if (flags & F_E8)
+                  ptx::tma_store_2d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0);
+              }
+              ptx::bulk_commit_group();
+              ptx::bulk_wait_group_read<1>();
+            }
+            if ((flags & F_AUX) && c + 2 < chunks) {
+              issue_aux(g + 2, n0 + (c + 2) * CHUNK, slab_row0);
+              aux_issued = g + 3;
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      gchunk += chunks;
+
+      // ---- row statistics: partial sums, then the last arriving warp of
+      // this row block turns them into 1/sqrt(mean + eps).
+      if (flags & F_ROW) {
+        if (row_ok) atomicAdd(p.row_out + m, row_ss);
+        __threadfence();
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) prev = atomicAdd(p.row_counter + mb, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == static_cast<uint32_t>(NUM_EPI_WARPS * p.num_n_tiles - 1)) {
+          __threadfence();
+          const float inv_n = 1.0f / static_cast<float>(p.n_out);
+          for (int r = lane; r < BLOCK_M; r += 32) {
+            const int mm = mb * BLOCK_M + r;
+            if (mm < p.M) {
+              const float ss = __ldcg(p.row_out + mm);
+              p.row_out[mm] = 1.0f / sqrtf(fmaf(ss, inv_n, p.rms_eps));
+            }
+          }
+        }
+      }
+    }
+
+    // ---- teardown of the epilogue warp
+    if (lane == 0) {
+      ptx::bulk_wait_group<0>();
+      // Aux loads still in flight after an abort land before the CTA exits.
+      for (uint32_t g = aux_done; g < aux_issued; ++g)
+        drain_wait(bar(BAR_AUX + ew * EPI_BUFS + g % EPI_BUFS), (g / EPI_BUFS) & 1u, p.timeout_ns);
+    }
+    if (flags & F_AMAX) {
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, s));
+      if (lane == 0 && amax_bits != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.amax), amax_bits);
+    }
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace ge

@@ -1,0 +1,525 @@
+// gemm_epi.cu -- host side of the C ABI in include/gemm_epi.h.
+//
+// create = validate the descriptor and the epilogue program, derive the
+// kernel flags (host only, no CUDA call).  run = check the device and the
+// pointer pack, zero the reduction outputs and the workspace with
+// cudaMemsetAsync, encode the TMA descriptors for this call's pointers and
+// launch the persistent kernel on the caller's stream.  This follows the
+// "build once, execute with a variant pack of pointers and a workspace" shape
+// of the cuDNN Graph API tutorial (five-step build paragraph); nothing here
+// allocates or synchronises, so a run can be captured in a CUDA graph (same
+// page, CUDA graph paragraph).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/gemm_epi.h"
+#include "fused_kernel.cuh"
+#include "unfused_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gemm_epi_status fail(gemm_epi_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+gemm_epi_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GEMM_EPI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t WS_HEADER = 256;  // status words; row counters follow
+constexpr int DEFAULT_GROUP_M = 16;
+constexpr uint32_t DEFAULT_TIMEOUT_MS = 2000;
+
+struct DeviceState {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[128];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+gemm_epi_status device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 128) return fail(GEMM_EPI_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (d.cc_major == 10 && d.cc_minor == 3) {
+      e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, ge::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(GEMM_EPI_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3)
+    return fail(GEMM_EPI_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                d.cc_major, d.cc_minor);
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return GEMM_EPI_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gemm_epi_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                         CUtensorMapSwizzle sw, CUtensorMapL2promotion l2, const char* what) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_EPI_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
+  return GEMM_EPI_OK;
+}
+
+bool is_output_op(int c) {
+  return c == GEMM_EPI_OP_AMAX || c == GEMM_EPI_OP_STORE_BF16 || c == GEMM_EPI_OP_STORE_E4M3 ||
+         c == GEMM_EPI_OP_ROW_RMS_RSQRT || c == GEMM_EPI_OP_COL_SUM;
+}
+
+bool is_pre_pair_op(int c) {
+  return c == GEMM_EPI_OP_SCALE_ALPHA || c == GEMM_EPI_OP_ADD_BIAS_COL || c == GEMM_EPI_OP_MUL_ROW_SCALE ||
+         c == GEMM_EPI_OP_ACT_GELU_TANH || c == GEMM_EPI_OP_ACT_RELU || c == GEMM_EPI_OP_ACT_SILU;
+}
+
+}  // namespace
+
+struct gemm_epi_plan {
+  gemm_epi_desc d;
+  std::vector<gemm_epi_op> ops;
+  int64_t n_out = 0;
+  int pair_at = -1, pair_g = 1;
+  uint32_t flags = 0;
+  bool uses_bias = false, uses_row_scale = false, uses_residual = false, uses_preact = false;
+  float rms_eps = 0.0f;
+  int rms_unrounded = 0;
+  int64_t num_m_tiles = 0, num_n_tiles = 0;
+  size_t ws_bytes = WS_HEADER;
+};
+
+namespace {
+
+gemm_epi_status validate(gemm_epi_plan& P) {
+  const gemm_epi_desc& d = P.d;
+  const int64_t LIM = 0x7FFFFFFF;
+  if (d.M < 0 || d.N < 0 || d.K < 0 || d.M > LIM || d.N > LIM || d.K > LIM)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "M, N, K must be in [0, 2^31)");
+  if (d.b_layout != GEMM_EPI_B_KN && d.b_layout != GEMM_EPI_B_NK)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "unknown b_layout %d", d.b_layout);
+  if (d.n_ops < 0 || d.n_ops > GEMM_EPI_MAX_OPS)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "n_ops must be in [0, %d]", GEMM_EPI_MAX_OPS);
+  if (d.n_ops > 0 && !d.ops) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ops is NULL");
+
+  int seen[16] = {0};
+  for (int i = 0; i < d.n_ops; ++i) {
+    const gemm_epi_op& op = d.ops[i];
+    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_COL_SUM)
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: unknown code %d", i, op.code);
+    if (is_output_op(op.code) && seen[op.code])
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: output op %d appears twice", i, op.code);
+    seen[op.code]++;
+    switch (op.code) {
+      case GEMM_EPI_OP_PAIR_SWIGLU: {
+        if (P.pair_at >= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU appears twice");
+        int g = op.i0 == 0 ? 1 : op.i0;
+        if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU group %d not in {1,2,4,8,16,32}", op.i0);
+        if (d.N % (2 * g) != 0)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU group %d needs N %% %d == 0 (N=%lld)", g,
+                      2 * g, static_cast<long long>(d.N));
+        for (int j = 0; j < i; ++j)
+          if (!is_pre_pair_op(d.ops[j].code))
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "op %d (code %d) before PAIR_SWIGLU is not supported", j,
+                        d.ops[j].code);
+        P.pair_at = i;
+        P.pair_g = g;
+        break;
+      }
+      case GEMM_EPI_OP_ROW_RMS_RSQRT:
+        if (!(op.f0 >= 0.0f) || !std::isfinite(op.f0))
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT eps must be finite and >= 0");
+        if (op.i0 != 0 && op.i0 != 1) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT mode must be 0 or 1");
+        P.rms_eps = op.f0;
+        P.rms_unrounded = op.i0;
+        P.flags |= ge::F_ROW;
+        break;
+      case GEMM_EPI_OP_ADD_BIAS_COL: P.uses_bias = true; break;
+      case GEMM_EPI_OP_MUL_ROW_SCALE: P.uses_row_scale = true; break;
+      case GEMM_EPI_OP_ADD_RESIDUAL: P.uses_residual = true; break;
+      case GEMM_EPI_OP_MUL_GELU_TANH_GRAD: P.uses_preact = true; break;
+      case GEMM_EPI_OP_AMAX: P.flags |= ge::F_AMAX; break;
+      case GEMM_EPI_OP_STORE_BF16: P.flags |= ge::F_STORE; break;
+      case GEMM_EPI_OP_STORE_E4M3: P.flags |= ge::F_E8; break;
+      case GEMM_EPI_OP_COL_SUM: P.flags |= ge::F_COL; break;
+      default: break;
+    }
+  }
+  if (P.uses_residual && P.uses_preact)
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "ADD_RESIDUAL and MUL_GELU_TANH_GRAD in one program need two "
+                                          "auxiliary tensors; this build reads one");
+  if (P.uses_residual || P.uses_preact) P.flags |= ge::F_AUX;
+  if (d.K == 0) P.flags |= ge::F_ZERO_ACC;
+  P.n_out = P.pair_at >= 0 ? d.N / 2 : d.N;
+  if ((P.flags & ge::F_ROW) && P.n_out == 0 && d.M > 0)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT over zero columns is undefined");
+
+  // Strides: bounds first, then the 16-byte TMA rule.
+  const bool kn = d.b_layout == GEMM_EPI_B_KN;
+  if (d.K > 0) {  // A and B are not read when K == 0
+    if (d.lda < d.K) return fail(GEMM_EPI_ERR_INVALID_VALUE, "lda < K");
+    if (d.ldb < (kn ? d.N : d.K) || d.ldb <= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldb too small");
+    if (d.lda % 8 || d.ldb % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "lda and ldb must be multiples of 8");
+  }
+  if ((P.flags & ge::F_STORE) && (d.ldc < P.n_out || d.ldc <= 0))
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldc < output columns");
+  if ((P.flags & ge::F_E8) && (d.ldc8 < P.n_out || d.ldc8 <= 0))
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldc8 < output columns");
+  if ((P.flags & ge::F_AUX) && (d.ld_aux < P.n_out || d.ld_aux <= 0))
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "ld_aux < output columns");
+  if ((P.flags & ge::F_STORE) && d.ldc % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "ldc must be a multiple of 8");
+  if ((P.flags & ge::F_E8) && d.ldc8 % 16) return fail(GEMM_EPI_ERR_MISALIGNED, "ldc8 must be a multiple of 16");
+  if ((P.flags & ge::F_AUX) && d.ld_aux % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "ld_aux must be a multiple of 8");
+  if (d.lda > (int64_t(1) << 38) || d.ldb > (int64_t(1) << 38) || d.ldc > (int64_t(1) << 38) ||
+      d.ldc8 > (int64_t(1) << 39) || d.ld_aux > (int64_t(1) << 38))
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "row stride beyond the TMA limit");
+
+  P.num_m_tiles = (d.M + ge::BLOCK_M - 1) / ge::BLOCK_M;
+  P.num_n_tiles = (d.N + ge::BLOCK_N - 1) / ge::BLOCK_N;
+  if (P.num_m_tiles * P.num_n_tiles > LIM) return fail(GEMM_EPI_ERR_INVALID_VALUE, "too many tiles");
+  P.ws_bytes = WS_HEADER + ((static_cast<size_t>(P.num_m_tiles) * 4 + 255) / 256) * 256;
+  return GEMM_EPI_OK;
+}
+
+struct Launch {
+  CUtensorMap ta, tb, tc, tc8, taux;
+  ge::KernelParams kp;
+  int grid;
+};
+
+// Fills the kernel parameters and tensor maps of one fused launch.  `c`/`ldc`
+// may differ from the plan's (the unfused baseline stores the bare
+// accumulator into its scratch buffer with a store-only program).
+gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const DeviceState& dev, Launch& L) {
+  const gemm_epi_desc& d = P.d;
+  std::memset(&L, 0, sizeof L);
+  ge::KernelParams& k = L.kp;
+  k.M = static_cast<int32_t>(d.M);
+  k.N = static_cast<int32_t>(d.N);
+  k.K = static_cast<int32_t>(d.K);
+  k.n_out = static_cast<int32_t>(P.n_out);
+  k.num_m_tiles = static_cast<int32_t>(P.num_m_tiles);
+  k.num_n_tiles = static_cast<int32_t>(P.num_n_tiles);
+  k.num_tiles = static_cast<int32_t>(P.num_m_tiles * P.num_n_tiles);
+  k.num_k_blocks = static_cast<int32_t>((d.K + ge::BLOCK_K - 1) / ge::BLOCK_K);
+  k.group_m = DEFAULT_GROUP_M;
+  k.b_kn = d.b_layout == GEMM_EPI_B_KN ? 1 : 0;
+  // Instruction descriptor: D fp32, A and B bf16, A K-major, B K- or
+  // MN-major, N = 256, M = 128.
+  k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (k.b_kn ? (1u << 16) : 0u) |
+            (static_cast<uint32_t>(ge::BLOCK_N >> 3) << 17) | (static_cast<uint32_t>(ge::BLOCK_M >> 4) << 24);
+  k.flags = P.flags;
+  k.n_ops = static_cast<int32_t>(P.ops.size());
+  k.pair_at = P.pair_at;
+  k.pair_g = P.pair_g;
+  k.alpha = a.alpha;
+  k.fp8_scale = a.fp8_scale;
+  k.rms_eps = P.rms_eps;
+  k.rms_unrounded = P.rms_unrounded;
+  k.bias = a.bias;
+  k.row_scale = a.row_scale;
+  k.amax = a.amax;
+  k.row_out = a.row_out;
+  k.col_out = a.col_out;
+  k.status = static_cast<uint32_t*>(a.workspace);
+  k.row_counter = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + WS_HEADER);
+  k.timeout_ns = static_cast<uint64_t>(a.timeout_ms ? a.timeout_ms : DEFAULT_TIMEOUT_MS) * 1000000ull;
+  k.debug_flags = a.debug_flags;
+  for (size_t i = 0; i < P.ops.size(); ++i) {
+    k.ops[i].code = P.ops[i].code;
+    k.ops[i].i0 = P.ops[i].i0;
+    k.ops[i].f0 = P.ops[i].f0;
+  }
+  L.grid = static_cast<int>(std::min<int64_t>(k.num_tiles, dev.sms));
+
+  gemm_epi_status s;
+  if (d.K > 0) {
+    s = make_map(&L.ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, d.K, d.M, d.lda * 2, ge::BLOCK_K, ge::BLOCK_M,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
+    if (s) return s;
+    if (k.b_kn)
+      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.N, d.K, d.ldb * 2, 64, ge::BLOCK_K,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
+    else
+      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.K, d.N, d.ldb * 2, ge::BLOCK_K, ge::BLOCK_N,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
+    if (s) return s;
+  }
+  if (P.flags & ge::F_STORE) {
+    s = make_map(&L.tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, P.n_out, d.M, d.ldc * 2, ge::CHUNK, 32,
+                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
+    if (s) return s;
+  }
+  if (P.flags & ge::F_E8) {
+    s = make_map(&L.tc8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.C8, P.n_out, d.M, d.ldc8, ge::CHUNK, 32,
+                 CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C8");
+    if (s) return s;
+  }
+  if (P.flags & ge::F_AUX) {
+    const void* aux = P.uses_residual ? a.residual : a.preact;
+    s = make_map(&L.taux, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, aux, P.n_out, d.M, d.ld_aux * 2, ge::CHUNK, 32,
+                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, "aux");
+    if (s) return s;
+  }
+  return GEMM_EPI_OK;
+}
+
+gemm_epi_status check_args(const gemm_epi_plan& P, const gemm_epi_args& a) {
+  const gemm_epi_desc& d = P.d;
+  const bool work = d.M > 0 && P.n_out > 0;
+  auto need = [&](const void* ptr, const char* name) -> gemm_epi_status {
+    if (!ptr) return fail(GEMM_EPI_ERR_INVALID_VALUE, "%s is NULL but the program uses it", name);
+    if (!aligned16(ptr)) return fail(GEMM_EPI_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    return GEMM_EPI_OK;
+  };
+  gemm_epi_status s;
+  if (work && d.K > 0) {
+    if ((s = need(a.A, "A")) || (s = need(a.B, "B"))) return s;
+  }
+  if (work) {
+    if ((P.flags & ge::F_STORE) && (s = need(a.C, "C"))) return s;
+    if ((P.flags & ge::F_E8) && (s = need(a.C8, "C8"))) return s;
+    if (P.uses_bias && (s = need(a.bias, "bias"))) return s;
+    if (P.uses_row_scale && (s = need(a.row_scale, "row_scale"))) return s;
+    if (P.uses_residual && (s = need(a.residual, "residual"))) return s;
+    if (P.uses_preact && (s = need(a.preact, "preact"))) return s;
+  }
+  if ((P.flags & ge::F_AMAX) && (s = need(a.amax, "amax"))) return s;
+  if ((P.flags & ge::F_ROW) && d.M > 0 && (s = need(a.row_out, "row_out"))) return s;
+  if ((P.flags & ge::F_COL) && P.n_out > 0 && (s = need(a.col_out, "col_out"))) return s;
+  if (!a.workspace || !aligned16(a.workspace) || a.workspace_bytes < P.ws_bytes)
+    return fail(GEMM_EPI_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",
+                P.ws_bytes, a.workspace ? a.workspace_bytes : static_cast<size_t>(0));
+  return GEMM_EPI_OK;
+}
+
+// Zeroes what the kernels accumulate into: status words and row counters,
+// amax, row sums, column sums.
+gemm_epi_status clear_outputs(const gemm_epi_plan& P, const gemm_epi_args& a, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(a.workspace, 0, P.ws_bytes, st);
+  if (e == cudaSuccess && (P.flags & ge::F_AMAX)) e = cudaMemsetAsync(a.amax, 0, sizeof(float), st);
+  if (e == cudaSuccess && (P.flags & ge::F_ROW) && P.d.M > 0)
+    e = cudaMemsetAsync(a.row_out, 0, sizeof(float) * P.d.M, st);
+  if (e == cudaSuccess && (P.flags & ge::F_COL) && P.n_out > 0)
+    e = cudaMemsetAsync(a.col_out, 0, sizeof(float) * P.n_out, st);
+  return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.blockDim = dim3(ge::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = ge::SMEM_BYTES;
+  cfg.stream = st;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
+  return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the fused kernel");
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_epi_status gemm_epi_create(gemm_epi_handle* out, const gemm_epi_desc* desc) {
+  g_last_error.clear();
+  if (!out || !desc) return fail(GEMM_EPI_ERR_INVALID_VALUE, "out and desc must not be NULL");
+  gemm_epi_plan* P = new (std::nothrow) gemm_epi_plan();
+  if (!P) return fail(GEMM_EPI_ERR_INVALID_VALUE, "out of host memory");
+  P->d = *desc;
+  if (desc->n_ops > 0 && desc->ops && desc->n_ops <= GEMM_EPI_MAX_OPS)
+    P->ops.assign(desc->ops, desc->ops + desc->n_ops);
+  P->d.ops = P->ops.data();
+  gemm_epi_status s = validate(*P);
+  if (s != GEMM_EPI_OK) {
+    delete P;
+    return s;
+  }
+  *out = P;
+  return GEMM_EPI_OK;
+}
+
+gemm_epi_status gemm_epi_destroy(gemm_epi_handle h) {
+  delete h;
+  return GEMM_EPI_OK;
+}
+
+size_t gemm_epi_workspace_size(gemm_epi_handle h) { return h ? h->ws_bytes : 0; }
+
+int64_t gemm_epi_out_cols(gemm_epi_handle h) { return h ? h->n_out : -1; }
+
+gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args* args, void* stream) {
+  g_last_error.clear();
+  if (!h || !args) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and args must not be NULL");
+  DeviceState* dev = nullptr;
+  gemm_epi_status s = device_state(&dev, nullptr);
+  if (s) return s;
+  if ((s = check_args(*h, *args))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = clear_outputs(*h, *args, st))) return s;
+  if (h->d.M == 0 || h->n_out == 0) return GEMM_EPI_OK;
+  Launch L;
+  if ((s = prepare(*h, *args, *dev, L))) return s;
+  return launch_fused(L, st);
+}
+
+gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* args, void* scratch,
+                                     int64_t ld_scratch, void* stream) {
+  g_last_error.clear();
+  if (!h || !args) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and args must not be NULL");
+  if (h->pair_at >= 0 && h->pair_g > 8)
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass handles PAIR_SWIGLU groups up to 8");
+  DeviceState* dev = nullptr;
+  gemm_epi_status s = device_state(&dev, nullptr);
+  if (s) return s;
+  if ((s = check_args(*h, *args))) return s;
+  const gemm_epi_desc& d = h->d;
+  if (d.M > 0 && d.N > 0) {
+    if (!scratch) return fail(GEMM_EPI_ERR_INVALID_VALUE, "scratch is NULL");
+    if (!aligned16(scratch)) return fail(GEMM_EPI_ERR_MISALIGNED, "scratch is not 16-byte aligned");
+    if (ld_scratch < d.N) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ld_scratch < N");
+    if (ld_scratch % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "ld_scratch must be a multiple of 8");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = clear_outputs(*h, *args, st))) return s;
+  if (d.M == 0 || h->n_out == 0) return GEMM_EPI_OK;
+
+  // 1) bare GEMM: the same kernel with a store-only program into scratch.
+  gemm_epi_plan bare;
+  bare.d = d;
+  bare.d.ldc = ld_scratch;
+  bare.ops.push_back(gemm_epi_op{GEMM_EPI_OP_STORE_BF16, 0, 0.0f});
+  bare.d.ops = bare.ops.data();
+  bare.d.n_ops = 1;
+  if ((s = validate(bare))) return s;
+  gemm_epi_args ba = *args;
+  ba.C = scratch;
+  Launch L;
+  if ((s = prepare(bare, ba, *dev, L))) return s;
+  if ((s = launch_fused(L, st))) return s;
+
+  // 2) the epilogue as a separate memory-bound pass over scratch.
+  ge::UnfusedParams u;
+  std::memset(&u, 0, sizeof u);
+  u.M = static_cast<int32_t>(d.M);
+  u.N = static_cast<int32_t>(d.N);
+  u.n_out = static_cast<int32_t>(h->n_out);
+  u.pair_at = h->pair_at;
+  u.pair_g = h->pair_g;
+  u.n_ops = static_cast<int32_t>(h->ops.size());
+  u.flags = h->flags;
+  u.alpha = args->alpha;
+  u.fp8_scale = args->fp8_scale;
+  u.rms_eps = h->rms_eps;
+  u.rms_unrounded = h->rms_unrounded;
+  u.acc = static_cast<const uint16_t*>(scratch);
+  u.ld_acc = ld_scratch;
+  u.aux = static_cast<const uint16_t*>(h->uses_residual ? args->residual : args->preact);
+  u.ld_aux = d.ld_aux;
+  u.bias = args->bias;
+  u.row_scale = args->row_scale;
+  u.c = static_cast<uint16_t*>(args->C);
+  u.ldc = d.ldc;
+  u.c8 = static_cast<uint8_t*>(args->C8);
+  u.ldc8 = d.ldc8;
+  u.amax = args->amax;
+  u.row_out = args->row_out;
+  u.col_out = args->col_out;
+  for (size_t i = 0; i < h->ops.size(); ++i) {
+    u.ops[i].code = h->ops[i].code;
+    u.ops[i].i0 = h->ops[i].i0;
+    u.ops[i].f0 = h->ops[i].f0;
+  }
+  dim3 grid(static_cast<unsigned>((h->n_out + ge::UF_COLS - 1) / ge::UF_COLS),
+            static_cast<unsigned>((d.M + ge::UF_ROWS - 1) / ge::UF_ROWS));
+  if (grid.y > 65535u) return fail(GEMM_EPI_ERR_UNSUPPORTED, "separate pass: M too large for its grid");
+  ge::unfused_epilogue_kernel<<<grid, ge::UF_THREADS, 0, st>>>(u);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch of the separate epilogue pass");
+  if (h->flags & ge::F_ROW) {
+    const int threads = 256;
+    ge::row_rms_finalize_kernel<<<static_cast<unsigned>((d.M + threads - 1) / threads), threads, 0, st>>>(
+        args->row_out, static_cast<int>(d.M), 1.0f / static_cast<float>(h->n_out), h->rms_eps);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch of the row finalize kernel");
+  }
+  return GEMM_EPI_OK;
+}
+
+gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void* workspace, void* stream) {
+  g_last_error.clear();
+  if (!h || !workspace) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and workspace must not be NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t words[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy of the status words");
+  if (words[0] & 1u)
+    return fail(GEMM_EPI_ERR_TIMEOUT, "in-kernel wait ran out (site %u, block %u)", words[1], words[2]);
+  return GEMM_EPI_OK;
+}
+
+const char* gemm_epi_status_string(gemm_epi_status s) {
+  switch (s) {
+    case GEMM_EPI_OK: return "ok";
+    case GEMM_EPI_ERR_INVALID_VALUE: return "invalid value";
+    case GEMM_EPI_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case GEMM_EPI_ERR_UNSUPPORTED: return "unsupported program";
+    case GEMM_EPI_ERR_ARCH: return "unsupported device architecture";
+    case GEMM_EPI_ERR_CUDA: return "CUDA error";
+    case GEMM_EPI_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case GEMM_EPI_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* gemm_epi_last_error(void) { return g_last_error.c_str(); }
+
+int gemm_epi_version(void) { return GEMM_EPI_VERSION; }
+
+}  // extern "C"

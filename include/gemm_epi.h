@@ -1,0 +1,211 @@
+/*
+ * gemm_epi.h -- C ABI of the GB300 (sm_103a) fused GEMM + epilogue engine.
+ *
+ * One call computes   acc = A @ B   (bf16 x bf16 -> fp32 accumulate, on the
+ * tcgen05 tensor cores) and, while each output tile is still on chip, runs a
+ * short epilogue program on it: scaling, bias, row scale, residual add,
+ * activations, a pairwise SwiGLU on interleaved gate/up columns, the GELU-tanh
+ * derivative, AMAX, row RMS statistics, column sums, and bf16 / FP8-e4m3
+ * stores.  Only the program's outputs reach global memory.
+ *
+ * Where the operations come from (page title, section):
+ *  - GEMM O = X @ W with tiling, shared-memory staging, a pipelined K loop,
+ *    swizzled tile order and tensor cores: "Lean4-TileLang Tensor Program
+ *    Superoptimizer" (itsolotime.com), section 8 "Matmul"; and "Toi uu hoa GPU
+ *    Kernel voi TileLang: Tu GEMM den FlashAttention" (aihot.vn), the tiled
+ *    tensor-core GEMM paragraph.
+ *  - bias + GELU applied to the register-resident accumulator before the
+ *    final store: the TileLang tutorial, fused GEMM epilogue paragraph.
+ *  - alpha given as a host scalar, bias, activation and an AMAX reduction in
+ *    the same kernel for the next FP8 quantisation: "Huong dan su dung NVIDIA
+ *    cuDNN Graph API" (aihot.vn), batched matmul epilogue paragraph.
+ *  - SwiGLU out = up * silu(gate): Superoptimizer, section 7 "SwiGLU".
+ *  - RMSNorm S = 1/sqrt(mean(x^2) + eps) and the row-broadcast rewrite
+ *    (X*S)@W = (X@W)*S: Superoptimizer, sections 3 and 9 "RMSNorm".
+ *  - a small set of composable epilogue primitives (scaling, reductions,
+ *    pairwise transforms, accumulation) finished on the on-chip output tile,
+ *    covering forward and backward work: "CODA: ... GEMM-Epilogue"
+ *    (lehuy.net), "How CODA works".
+ *  - create once (validate + plan), then execute with a pack of pointers and
+ *    a caller-owned workspace: cuDNN Graph API tutorial, five-step build
+ *    paragraph; launches are safe to capture in a CUDA graph (same page, CUDA
+ *    graph paragraph).
+ *
+ * Memory and ownership
+ *  - Every pointer in gemm_epi_args is a DEVICE pointer the caller allocated
+ *    and owns (the workspace included).  The library owns only the host-side
+ *    plan behind a gemm_epi_handle.
+ *  - gemm_epi_run allocates nothing and never synchronises: it enqueues
+ *    cudaMemsetAsync calls (reduction outputs and the workspace) and one
+ *    kernel launch on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Reduction outputs (amax, row_out, col_out) are OVERWRITTEN by each run,
+ *    never accumulated across calls.
+ *
+ * Layouts (all row-major, strides in elements unless stated)
+ *  - A: M x K bf16, row stride lda >= K.
+ *  - B: GEMM_EPI_B_KN: K x N bf16, row stride ldb >= N;
+ *       GEMM_EPI_B_NK: N x K bf16 (B = W^T for a weight W stored N x K),
+ *       row stride ldb >= K.
+ *  - Output columns: N_out = N, or N/2 after GEMM_EPI_OP_PAIR_SWIGLU.
+ *  - C: M x N_out bf16, row stride ldc >= N_out.  C8: M x N_out e4m3 bytes,
+ *    row stride ldc8 >= N_out (bytes).
+ *  - residual / preact: M x N_out bf16, row stride ld_aux >= N_out.
+ *  - bias: fp32, N_out values (N values when the op sits before the pair op).
+ *  - row_scale: fp32, M values.  amax: 1 fp32.  row_out: M fp32.
+ *    col_out: N_out fp32.
+ *  - TMA needs every base pointer 16-byte aligned and every row stride a
+ *    multiple of 16 bytes (8 bf16 elements, 16 e4m3 bytes); anything else is
+ *    GEMM_EPI_ERR_MISALIGNED.
+ *
+ * Errors
+ *  - create / run return synchronous validation errors and never launch
+ *    anything when they fail; gemm_epi_last_error() gives a one-line reason
+ *    (thread-local, valid until the next call on the same thread).
+ *  - Every wait inside the kernel is bounded (timeout_ms).  A wait that runs
+ *    out sets a status word in the workspace, the kernel drains what it has in
+ *    flight, frees its tensor memory and returns; gemm_epi_query_status
+ *    reports GEMM_EPI_ERR_TIMEOUT.  The kernel never traps.
+ */
+#ifndef GEMM_EPI_H
+#define GEMM_EPI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_EPI_VERSION 1
+
+typedef enum gemm_epi_status {
+    GEMM_EPI_OK = 0,
+    GEMM_EPI_ERR_INVALID_VALUE = 1, /* bad size, NULL where required, bad program */
+    GEMM_EPI_ERR_MISALIGNED = 2,    /* pointer or stride breaks the 16-byte TMA rule */
+    GEMM_EPI_ERR_UNSUPPORTED = 3,   /* a legal program this build does not implement */
+    GEMM_EPI_ERR_ARCH = 4,          /* current device is not compute capability 10.x */
+    GEMM_EPI_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
+    GEMM_EPI_ERR_TIMEOUT = 6,       /* a bounded in-kernel wait ran out */
+    GEMM_EPI_ERR_WORKSPACE = 7      /* workspace missing or smaller than required */
+} gemm_epi_status;
+
+typedef enum gemm_epi_b_layout {
+    GEMM_EPI_B_KN = 0, /* B stored K x N row-major (N contiguous) */
+    GEMM_EPI_B_NK = 1  /* B stored N x K row-major (K contiguous), i.e. W^T */
+} gemm_epi_b_layout;
+
+/*
+ * Epilogue primitives.  The program is applied per output element, in order,
+ * to a running fp32 value y that starts as acc[m, n].  Element-wise ops
+ * transform y; output ops record y and leave it unchanged.
+ */
+typedef enum gemm_epi_op_code {
+    GEMM_EPI_OP_SCALE_ALPHA = 1,        /* y = alpha * y            (args.alpha)            */
+    GEMM_EPI_OP_ADD_BIAS_COL = 2,       /* y = y + bias[n]          (args.bias)             */
+    GEMM_EPI_OP_MUL_ROW_SCALE = 3,      /* y = y * row_scale[m]     (args.row_scale)        */
+    GEMM_EPI_OP_ADD_RESIDUAL = 4,       /* y = y + residual[m, n]   (args.residual)         */
+    GEMM_EPI_OP_ACT_GELU_TANH = 5,      /* y = gelu_tanh(y)                                 */
+    GEMM_EPI_OP_ACT_RELU = 6,           /* y = max(y, 0)                                    */
+    GEMM_EPI_OP_ACT_SILU = 7,           /* y = y * sigmoid(y)                               */
+    GEMM_EPI_OP_PAIR_SWIGLU = 8,        /* y'[m,j] = silu(y[m,gate(j)]) * y[m,up(j)];
+                                           i0 = group g in {1,2,4,8,16,32} (0 means 1):
+                                           gate(j) = (j/g)*2g + j%g, up(j) = gate(j) + g;
+                                           g = 1 is even = gate, odd = up.  N_out = N/2.  */
+    GEMM_EPI_OP_MUL_GELU_TANH_GRAD = 9, /* y = y * gelu_tanh'(preact[m, n]) (args.preact)    */
+    GEMM_EPI_OP_AMAX = 10,              /* *amax = max over valid (m,n) of |y|               */
+    GEMM_EPI_OP_STORE_BF16 = 11,        /* C[m, n] = bf16_rne(y)                             */
+    GEMM_EPI_OP_STORE_E4M3 = 12,        /* C8[m, n] = e4m3_rne_satfinite(y * args.fp8_scale) */
+    GEMM_EPI_OP_ROW_RMS_RSQRT = 13,     /* row_out[m] = 1/sqrt(mean_n(v^2) + f0), f0 = eps;
+                                           v = bf16_rne(y) when i0 == 0, v = y when i0 == 1 */
+    GEMM_EPI_OP_COL_SUM = 14            /* col_out[n] = sum over m of y                      */
+} gemm_epi_op_code;
+
+typedef struct gemm_epi_op {
+    int32_t code; /* gemm_epi_op_code */
+    int32_t i0;   /* integer argument (see the op) */
+    float f0;     /* float argument (see the op) */
+} gemm_epi_op;
+
+#define GEMM_EPI_MAX_OPS 16
+
+typedef struct gemm_epi_desc {
+    int64_t M, N, K;          /* GEMM sizes; M, N >= 0, K >= 0 (K == 0: acc = 0) */
+    int64_t lda, ldb;         /* row strides of A and B, elements */
+    int64_t ldc;              /* row stride of C (bf16 elements); used with STORE_BF16 */
+    int64_t ldc8;             /* row stride of C8 (bytes); used with STORE_E4M3 */
+    int64_t ld_aux;           /* row stride of residual / preact (elements) */
+    int32_t b_layout;         /* gemm_epi_b_layout */
+    int32_t n_ops;            /* 0 .. GEMM_EPI_MAX_OPS */
+    const gemm_epi_op *ops;   /* copied by gemm_epi_create */
+} gemm_epi_desc;
+
+typedef struct gemm_epi_args {
+    const void *A;            /* bf16, device */
+    const void *B;            /* bf16, device */
+    float alpha;              /* SCALE_ALPHA */
+    float fp8_scale;          /* STORE_E4M3 */
+    const float *bias;        /* ADD_BIAS_COL */
+    const float *row_scale;   /* MUL_ROW_SCALE */
+    const void *residual;     /* ADD_RESIDUAL, bf16 */
+    const void *preact;       /* MUL_GELU_TANH_GRAD, bf16 */
+    void *C;                  /* STORE_BF16 output */
+    void *C8;                 /* STORE_E4M3 output */
+    float *amax;              /* AMAX output, 1 value */
+    float *row_out;           /* ROW_RMS_RSQRT output, M values */
+    float *col_out;           /* COL_SUM output, N_out values */
+    void *workspace;          /* gemm_epi_workspace_size(h) bytes, 16-byte aligned */
+    size_t workspace_bytes;
+    uint32_t timeout_ms;      /* bound of every in-kernel wait; 0 = 2000 ms */
+    uint32_t debug_flags;     /* 0 in normal use; GEMM_EPI_DEBUG_* for tests */
+} gemm_epi_args;
+
+/* Test hook: the producer skips the first operand load of the first CTA so
+ * that the consumer's bounded wait runs out (nothing is left in flight). */
+#define GEMM_EPI_DEBUG_SKIP_FIRST_LOAD 1u
+
+typedef struct gemm_epi_plan *gemm_epi_handle;
+
+/* Validates the descriptor and builds a host-side plan.  Pure host code: no
+ * CUDA call, no device needed.  *out is set only on GEMM_EPI_OK. */
+gemm_epi_status gemm_epi_create(gemm_epi_handle *out, const gemm_epi_desc *desc);
+
+/* Frees the plan.  NULL is accepted. */
+gemm_epi_status gemm_epi_destroy(gemm_epi_handle h);
+
+/* Bytes of device workspace gemm_epi_run needs for this plan (>= 256). */
+size_t gemm_epi_workspace_size(gemm_epi_handle h);
+
+/* Output columns of the plan (N, or N/2 after PAIR_SWIGLU); -1 for NULL. */
+int64_t gemm_epi_out_cols(gemm_epi_handle h);
+
+/* Enqueues the fused kernel on `stream`.  Checks the device (compute
+ * capability 10.x), every pointer the program uses (non-NULL, 16-byte
+ * aligned) and the workspace.  Asynchronous; capture-safe. */
+gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
+
+/* The unfused baseline with the same semantics: a bare GEMM into `scratch`
+ * (M x N bf16 pre-epilogue accumulator, row stride ld_scratch >= N, caller
+ * owned), then a separate memory-bound epilogue pass that reads it back.  The
+ * accumulator is rounded to bf16 between the two, so results differ from the
+ * fused path by that rounding.  For measurement only. */
+gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args *args,
+                                     void *scratch, int64_t ld_scratch, void *stream);
+
+/* Synchronises `stream`, then reads the status word the last run on that
+ * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
+gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
+
+/* Static description of a status code. */
+const char *gemm_epi_status_string(gemm_epi_status s);
+
+/* One-line reason for the most recent failure on this thread ("" if none). */
+const char *gemm_epi_last_error(void);
+
+/* GEMM_EPI_VERSION of the loaded library. */
+int gemm_epi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_EPI_H */

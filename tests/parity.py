@@ -1,0 +1,144 @@
+"""Comparison rules between the CUDA path and the fp64 oracle.
+
+Tolerances (as the benchmark statement fixes them, with the readings noted):
+  bf16 outputs   |g - r| <= 2e-2 * max(|r|, 1e-2 * RMS(r))   (relative error
+                 2e-2, floored at 1% of the tensor RMS so that zero crossings
+                 of GELU / ReLU / gelu' do not divide by ~0)
+  fp32 rows      relative 1e-3
+  fp32 columns   |g - r| <= 1e-3 * sum_m |y[m, n]|
+  AMAX           within one bf16 ulp of r
+  e4m3 codes     identical, except two adjacent codes when the fp64 value lies
+                 within one bf16 ulp (2^-8 relative) of the midpoint between them
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from gemm_epilogue_transformer_smem_gb300 import api, synth
+
+BF16_TOL = 2e-2
+RED_TOL = 1e-3
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return synth.bf16_bits(t)
+
+
+def check_bf16(got_bits: np.ndarray, ref: np.ndarray, what="C"):
+    g = oracle.bf16_bits_to_f64(got_bits)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    if ref.size == 0:
+        return
+    rms = math.sqrt(float(np.mean(ref * ref)))
+    bound = BF16_TOL * np.maximum(np.abs(ref), 1e-2 * rms)
+    err = np.abs(g - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError("%s: %d of %d elements outside tolerance; first %s: got %s want %s" % (
+            what, int(bad.sum()), bad.size, idx.tolist(), g[tuple(idx.T)].tolist(),
+            ref[tuple(idx.T)].tolist()))
+
+
+def check_e4m3(got: np.ndarray, want_codes: np.ndarray, ref_scaled: np.ndarray):
+    got = np.asarray(got, dtype=np.uint8)
+    want = np.asarray(want_codes, dtype=np.uint8)
+    assert got.shape == want.shape
+    zero = lambda c: (c & 0x7F) == 0
+    diff = (got != want) & ~(zero(got) & zero(want))
+    if not diff.any():
+        return 0
+    for idx in np.argwhere(diff):
+        i = tuple(idx)
+        dg = float(oracle.e4m3_to_f64([got[i]])[0])
+        dw = float(oracle.e4m3_to_f64([want[i]])[0])
+        r = float(ref_scaled[i])
+        lo, hi = min(dg, dw), max(dg, dw)
+        # adjacent: no representable value strictly between them
+        between = oracle.to_e4m3([(lo + hi) / 2])[0]
+        mid = (lo + hi) / 2
+        adjacent = oracle.e4m3_to_f64([between])[0] in (lo, hi)
+        near = abs(r - mid) <= 2.0 ** -8 * max(abs(mid), 2.0 ** -9)
+        assert adjacent and near, "e4m3 code %s: got %#x want %#x for value %r" % (
+            i, got[i], want[i], r)
+    return int(diff.sum())
+
+
+def bf16_ulp(x: float) -> float:
+    if x == 0:
+        return 2.0 ** -133
+    return 2.0 ** (math.floor(math.log2(abs(x))) - 7)
+
+
+def check_amax(got: float, ref: float):
+    assert abs(got - ref) <= bf16_ulp(ref), (got, ref)
+
+
+def check_rows(got: np.ndarray, ref: np.ndarray):
+    np.testing.assert_allclose(np.asarray(got, np.float64), ref, rtol=RED_TOL, atol=0)
+
+
+def check_cols(got: np.ndarray, ref: np.ndarray, abs_sum: np.ndarray):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    bad = err > RED_TOL * abs_sum
+    assert not bad.any(), "column sums: %d bad, first %s" % (int(bad.sum()), np.argwhere(bad)[:5].tolist())
+
+
+# ------------------------------------------------------------------ running
+
+def oracle_problem(w: synth.Workload, inp: synth.Inputs) -> oracle.Problem:
+    prog = list(w.program)
+    aux = bits(inp.aux) if inp.aux is not None else None
+    return oracle.Problem(
+        A=bits(inp.A), B=bits(inp.B), program=prog, b_is_nk=(w.b_layout == "nk"),
+        alpha=inp.alpha, bias=None if inp.bias is None else inp.bias.detach().cpu().numpy(),
+        residual=aux if w.aux == "residual" else None,
+        preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale)
+
+
+def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout)
+    out = api.allocate_outputs(plan, inp.A.device)
+    scratch = None
+    if unfused:
+        scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=inp.A.device)
+    api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
+                    bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, **kw)
+    torch.cuda.synchronize()
+    status = plan.query_status(out.workspace)
+    assert status == 0, "kernel status %d" % status
+    return plan, out
+
+
+def compare_rows(w, inp, out, rows=None, oracle_p=None):
+    """Full output rows (all columns) of the listed rows, every output the
+    program has; `rows` None = all rows."""
+    p = oracle_p or oracle_problem(w, inp)
+    ref = p.rows(rows)
+    sel = slice(None) if rows is None else torch.as_tensor(np.asarray(rows), device=out.workspace.device)
+    prog = [op.partition(":")[0] for op in w.program]
+    if out.C is not None:
+        check_bf16(bits(out.C[sel]), ref["y"], "C")
+    if out.C8 is not None:
+        check_e4m3(out.C8[sel].cpu().numpy(), ref["c_e4m3"], ref["y"] * inp.fp8_scale)
+    if out.row_out is not None:
+        check_rows(out.row_out[sel].cpu().numpy(), ref["row_stat"])
+    if "amax" in prog and rows is None:
+        check_amax(float(out.amax.item()), ref["amax"])
+    return ref
+
+
+def compare_cols(w, inp, out, cols, oracle_p=None):
+    p = oracle_p or oracle_problem(w, inp)
+    ref = p.cols(cols)
+    idx = torch.as_tensor(np.asarray(cols), device=out.workspace.device)
+    if out.C is not None:
+        check_bf16(bits(out.C[:, idx]), ref["y"], "C columns")
+    if out.col_out is not None:
+        check_cols(out.col_out[idx].cpu().numpy(), ref["col_stat"], np.abs(ref["y"]).sum(0))
+    return ref

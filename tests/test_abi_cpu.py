@@ -1,0 +1,154 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/gemm_epi.h declares, and validates descriptors on the host
+(gemm_epi_create does no CUDA call).  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gemm_epilogue_transformer_smem_gb300 import api, build, native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_epi.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return N.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_epi_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", N.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (gemm_epi_\w+)", out))
+    assert set(names) <= exported, set(names) - exported
+    # the binding covers the same set
+    assert set(names) == {s[0] for s in N.SIGNATURES}
+
+
+def test_struct_layouts_match_header(lib):
+    assert ctypes.sizeof(N.gemm_epi_op) == 12
+    assert ctypes.sizeof(N.gemm_epi_desc) == 8 * 8 + 4 + 4 + 8
+    assert ctypes.sizeof(N.gemm_epi_args) == 2 * 8 + 2 * 4 + 10 * 8 + 8 + 2 * 4
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gemm_epi_version() == 1
+    for code in range(8):
+        assert lib.gemm_epi_status_string(code)
+    assert lib.gemm_epi_status_string(99) == b"unknown status"
+
+
+def create(lib, M=256, N_=512, K=128, program=("store_bf16",), layout=N.GEMM_EPI_B_KN, **strides):
+    ops = api.encode_program(list(program))
+    d = N.gemm_epi_desc()
+    d.M, d.N, d.K = M, N_, K
+    pair = any(p.startswith("pair") for p in program)
+    n_out = N_ // 2 if pair else N_
+    d.lda = strides.get("lda", K)
+    d.ldb = strides.get("ldb", N_ if layout == N.GEMM_EPI_B_KN else K)
+    d.ldc = strides.get("ldc", n_out)
+    d.ldc8 = strides.get("ldc8", n_out)
+    d.ld_aux = strides.get("ld_aux", n_out)
+    d.b_layout = layout
+    d.n_ops = strides.get("n_ops", len(program))
+    d.ops = ctypes.cast(ops, ctypes.POINTER(N.gemm_epi_op))
+    h = N.gemm_epi_handle()
+    s = lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d))
+    return s, h
+
+
+@pytest.mark.parametrize("program", [
+    ("store_bf16",),
+    ("alpha", "bias", "gelu_tanh", "amax", "store_bf16"),
+    ("pair_swiglu", "store_bf16"),
+    ("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"),
+    ("residual", "store_bf16", "row_rms:1e-6"),
+    ("gelu_tanh_grad", "store_bf16", "col_sum"),
+    (),
+])
+def test_create_accepts_programs(lib, program):
+    s, h = create(lib, program=program)
+    assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
+    pair = any(p.startswith("pair") for p in program)
+    assert lib.gemm_epi_out_cols(h) == (256 if pair else 512)
+    ws = lib.gemm_epi_workspace_size(h)
+    assert ws >= 256 and ws % 256 == 0
+    assert lib.gemm_epi_destroy(h) == N.GEMM_EPI_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(K=2 ** 31), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(layout=7), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(lda=64), N.GEMM_EPI_ERR_INVALID_VALUE),          # lda < K
+    (dict(lda=132), N.GEMM_EPI_ERR_MISALIGNED),            # not a multiple of 8
+    (dict(ldb=516), N.GEMM_EPI_ERR_MISALIGNED),
+    (dict(ldc=500), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(ldc=516), N.GEMM_EPI_ERR_MISALIGNED),
+    (dict(program=("store_bf16", "store_e4m3"), ldc8=520), N.GEMM_EPI_ERR_MISALIGNED),
+    (dict(program=("store_bf16", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("pair_swiglu", "pair_swiglu")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("pair_swiglu:3", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(N_=511, program=("pair_swiglu", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(N_=520, program=("pair_swiglu:8", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("residual", "pair_swiglu", "store_bf16")), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("store_bf16", "pair_swiglu")), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("residual", "gelu_tanh_grad", "store_bf16")), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("residual", "store_bf16"), ld_aux=12), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(N_=0, program=("row_rms",)), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("store_bf16",), n_ops=17), N.GEMM_EPI_ERR_INVALID_VALUE),
+])
+def test_create_rejects(lib, kw, status):
+    s, h = create(lib, **kw)
+    assert s == status, (s, lib.gemm_epi_last_error())
+    assert lib.gemm_epi_last_error()
+    assert not h.value
+
+
+def test_create_rejects_unknown_op_and_nulls(lib):
+    bad = (N.gemm_epi_op * 1)(N.gemm_epi_op(99, 0, 0.0))
+    d = N.gemm_epi_desc(M=8, N=8, K=8, lda=8, ldb=8, ldc=8, ldc8=16, ld_aux=8, b_layout=0, n_ops=1,
+                        ops=ctypes.cast(bad, ctypes.POINTER(N.gemm_epi_op)))
+    h = N.gemm_epi_handle()
+    assert lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)) == N.GEMM_EPI_ERR_INVALID_VALUE
+    assert lib.gemm_epi_create(None, ctypes.byref(d)) == N.GEMM_EPI_ERR_INVALID_VALUE
+    assert lib.gemm_epi_create(ctypes.byref(h), None) == N.GEMM_EPI_ERR_INVALID_VALUE
+    d.n_ops, d.ops = 2, None
+    assert lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)) == N.GEMM_EPI_ERR_INVALID_VALUE
+    assert lib.gemm_epi_destroy(None) == N.GEMM_EPI_OK
+    assert lib.gemm_epi_workspace_size(None) == 0
+    assert lib.gemm_epi_out_cols(None) == -1
+
+
+def test_zero_k_needs_no_operand_strides(lib):
+    s, h = create(lib, K=0, lda=0, program=("bias", "store_bf16"))
+    assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
+    lib.gemm_epi_destroy(h)
+
+
+def test_workspace_grows_with_row_tiles(lib):
+    s1, h1 = create(lib, M=128, program=("residual", "store_bf16", "row_rms"))
+    s2, h2 = create(lib, M=128 * 200, program=("residual", "store_bf16", "row_rms"))
+    assert s1 == s2 == N.GEMM_EPI_OK
+    assert lib.gemm_epi_workspace_size(h2) >= 256 + 4 * 200 > lib.gemm_epi_workspace_size(h1) - 1
+    lib.gemm_epi_destroy(h1)
+    lib.gemm_epi_destroy(h2)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        N.load(str(tmp_path / "nope.so"))

@@ -1,0 +1,282 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300).
+
+Small shapes are compared element by element in full; they span several
+128 x 256 tiles and leave ragged M, N and K tails.  The five benchmark
+workloads run at their full sizes, in the launch configuration the bench
+times, and are compared on sampled whole rows and whole columns plus
+invariants that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_epilogue_transformer_smem_gb300 import api, native, synth
+
+from parity import (bits, check_amax, check_bf16, check_cols, check_rows, compare_cols,
+                    compare_rows, oracle_problem, run_cuda)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+W = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return cuda_lib
+
+
+def small(name, M, N, K):
+    return W[name].scaled(M, N, K)
+
+
+# ------------------------------------------------------------ full compare, small
+
+SMALL_SHAPES = [
+    ("tiny", 64, 64, 128),          # the tiny workload itself (one partial tile)
+    ("tiny", 300, 600, 200),        # 3 x 3 tiles, ragged M, N and K tails
+    ("swiglu", 260, 1040, 136),     # pair op, 5 N tiles with a 16-column tail
+    ("fp8", 257, 520, 264),         # FP8 store + AMAX, K tail of 8
+    ("downproj", 384, 1000, 328),   # residual + row RMS across 4 N tiles
+    ("backward", 200, 776, 192),    # B stored N x K, gelu' + column sums
+]
+
+
+@pytest.mark.parametrize("name,M,N,K", SMALL_SHAPES)
+def test_small_full_compare(name, M, N, K):
+    w = small(name, M, N, K) if (M, N, K) != (W[name].M, W[name].N, W[name].K) else W[name]
+    inp = synth.make_inputs(w, DEV)
+    plan, out = run_cuda(w, inp)
+    compare_rows(w, inp, out)
+    if out.col_out is not None:
+        compare_cols(w, inp, out, list(range(w.n_out)))
+
+
+@pytest.mark.parametrize("name,M,N,K", SMALL_SHAPES[1:])
+def test_small_unfused_baseline(name, M, N, K):
+    w = small(name, M, N, K)
+    inp = synth.make_inputs(w, DEV)
+    plan, out = run_cuda(w, inp, unfused=True)
+    compare_rows(w, inp, out)
+    if out.col_out is not None:
+        compare_cols(w, inp, out, list(range(w.n_out)))
+
+
+@pytest.mark.parametrize("program,layout", [
+    (("store_bf16",), "kn"),
+    (("store_bf16",), "nk"),
+    (("alpha", "bias", "silu", "store_bf16"), "nk"),
+    (("row_scale", "gelu_tanh", "amax", "store_bf16"), "kn"),
+    (("alpha", "bias", "pair_swiglu", "store_bf16", "amax"), "kn"),
+    (("pair_swiglu:4", "store_bf16"), "kn"),
+    (("pair_swiglu:32", "relu", "store_bf16", "col_sum"), "nk"),
+    (("residual", "gelu_tanh", "store_bf16", "store_e4m3", "row_rms_unrounded:1e-5"), "nk"),
+    (("gelu_tanh_grad", "amax", "store_bf16", "col_sum", "row_rms"), "kn"),
+])
+def test_program_variants(program, layout):
+    aux = "residual" if "residual" in program else ("preact" if "gelu_tanh_grad" in program else None)
+    w = synth.Workload("variant", 11, 200, 512 + 64, 136, layout, program, a_std=0.3, b_std=0.3,
+                       bias_std=0.1 if "bias" in program else None, aux=aux, alpha=0.75, fp8_scale=64.0)
+    inp = synth.make_inputs(w, DEV, seed=77)
+    row_scale = torch.rand(w.M, device=DEV) + 0.5
+    plan = api.Plan(w.M, w.N, w.K, program, b_layout=layout)
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias,
+                    row_scale=row_scale, aux=inp.aux)
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    p = oracle_problem(w, inp)
+    p.row_scale = row_scale.cpu().numpy()
+    compare_rows(w, inp, out, oracle_p=p)
+    if out.col_out is not None:
+        compare_cols(w, inp, out, list(range(w.n_out)), oracle_p=p)
+
+
+# ------------------------------------------------------------ exact pins on the GPU
+
+def test_integer_inputs_bit_exact():
+    """Small integers keep the fp32 accumulation exact, and |C| <= 256 keeps
+    the bf16 store exact: any difference is a bug."""
+    g = torch.Generator(device=DEV).manual_seed(5)
+    M, N, K = 256, 512, 320
+    A = torch.randint(-2, 3, (M, K), generator=g, device=DEV).to(torch.bfloat16)
+    B = torch.randint(-2, 3, (K, N), generator=g, device=DEV).to(torch.bfloat16)
+    plan = api.Plan(M, N, K, ["store_bf16"])
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out)
+    torch.cuda.synchronize()
+    ref = oracle.Problem(bits(A), bits(B), ["store_bf16"]).rows()
+    assert np.abs(ref["y"]).max() <= 256
+    assert np.array_equal(bits(out.C), ref["c_bf16"])
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_identity_and_permutation(layout):
+    K, N = 256, 384
+    g = torch.Generator(device=DEV).manual_seed(6)
+    B = torch.randn((K, N) if layout == "kn" else (N, K), generator=g, device=DEV).to(torch.bfloat16)
+    Bkn = B if layout == "kn" else B.t().contiguous()
+    perm = torch.randperm(K, generator=g, device=DEV)
+    for A in (torch.eye(K, device=DEV, dtype=torch.bfloat16),
+              torch.eye(K, device=DEV, dtype=torch.bfloat16)[perm]):
+        plan = api.Plan(K, N, K, ["store_bf16"], b_layout=layout)
+        out = api.allocate_outputs(plan, DEV)
+        api.run_program(plan, A, B, out)
+        torch.cuda.synchronize()
+        want = (A.float() @ Bkn.float()).to(torch.bfloat16)  # exact: one nonzero per row
+        assert torch.equal(out.C.view(torch.int16), want.view(torch.int16))
+
+
+def test_row_scale_rewrite_identity():
+    """(X*S)@W == (X@W)*S for a row-broadcast S (powers of two: exact)."""
+    g = torch.Generator(device=DEV).manual_seed(8)
+    M, N, K = 300, 512, 192
+    X = torch.randn(M, K, generator=g, device=DEV).to(torch.bfloat16)
+    Wt = torch.randn(K, N, generator=g, device=DEV).to(torch.bfloat16)
+    S = torch.pow(2.0, torch.randint(-3, 4, (M,), generator=g, device=DEV).float())
+    p1 = api.Plan(M, N, K, ["store_bf16"])
+    o1 = api.allocate_outputs(p1, DEV)
+    api.run_program(p1, (X.float() * S[:, None]).to(torch.bfloat16), Wt, o1)
+    p2 = api.Plan(M, N, K, ["row_scale", "store_bf16"])
+    o2 = api.allocate_outputs(p2, DEV)
+    api.run_program(p2, X, Wt, o2, row_scale=S)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.C.view(torch.int16), o2.C.view(torch.int16))
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 256, 8), (127, 264, 64), (129, 8, 72), (64, 64, 0)])
+def test_edge_shapes(M, N, K):
+    w = synth.Workload("edge", 12, M, N, K, "kn", ("alpha", "bias", "gelu_tanh", "amax", "store_bf16"),
+                       a_std=0.5, b_std=0.5, bias_std=0.1, alpha=1.5)
+    inp = synth.make_inputs(w, DEV, seed=99)
+    plan, out = run_cuda(w, inp)
+    compare_rows(w, inp, out)
+
+
+def test_empty_problem_clears_reductions():
+    plan = api.Plan(0, 64, 64, ["amax", "store_bf16", "col_sum"])
+    out = api.allocate_outputs(plan, DEV)
+    out.amax.fill_(7.0)
+    out.col_out.fill_(7.0)
+    A = torch.empty((0, 64), device=DEV, dtype=torch.bfloat16)
+    B = torch.zeros((64, 64), device=DEV, dtype=torch.bfloat16)
+    plan.run(A, B, C=out.C, amax=out.amax, col_out=out.col_out, workspace=out.workspace)
+    torch.cuda.synchronize()
+    assert out.amax.item() == 0.0 and torch.all(out.col_out == 0)
+
+
+def test_strided_operands_and_guard_bands():
+    """Row strides larger than the logical width; sentinels beyond every
+    declared extent must survive."""
+    M, N, K = 200, 300, 136
+    lda, ldb, ldc = K + 24, N + 20, N + 36
+    g = torch.Generator(device=DEV).manual_seed(3)
+    Abuf = torch.randn(M, lda, generator=g, device=DEV).to(torch.bfloat16)
+    Bbuf = torch.randn(K, ldb, generator=g, device=DEV).to(torch.bfloat16)
+    Cbuf = torch.full((M + 3, ldc), 12345.0, device=DEV).to(torch.bfloat16)
+    sentinel = Cbuf[0, 0].clone()
+    plan = api.Plan(M, N, K, ["gelu_tanh", "store_bf16"], lda=lda, ldb=ldb, ldc=ldc)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
+    plan.run(Abuf, Bbuf, C=Cbuf, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.query_status(ws) == 0
+    assert torch.all(Cbuf[:M, N:] == sentinel) and torch.all(Cbuf[M:] == sentinel)
+    ref = oracle.Problem(bits(Abuf[:, :K]), bits(Bbuf[:, :N]), ["gelu_tanh", "store_bf16"]).rows()
+    check_bf16(bits(Cbuf[:M, :N]), ref["y"])
+
+
+def test_misaligned_and_missing_buffers_rejected():
+    plan = api.Plan(128, 256, 64, ["store_bf16", "amax"])
+    out = api.allocate_outputs(plan, DEV)
+    A = torch.zeros(128 * 64 + 8, device=DEV, dtype=torch.bfloat16)
+    B = torch.zeros(64, 256, device=DEV, dtype=torch.bfloat16)
+    with pytest.raises(native.GemmEpiError) as e:
+        plan.run(A[1:], B, C=out.C, amax=out.amax, workspace=out.workspace)
+    assert e.value.status == native.GEMM_EPI_ERR_MISALIGNED
+    with pytest.raises(native.GemmEpiError) as e:
+        plan.run(A, B, C=out.C, amax=None, workspace=out.workspace)
+    assert e.value.status == native.GEMM_EPI_ERR_INVALID_VALUE
+    with pytest.raises(native.GemmEpiError) as e:
+        plan.run(A, B, C=out.C, amax=out.amax, workspace=out.workspace[:16])
+    assert e.value.status == native.GEMM_EPI_ERR_WORKSPACE
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A load the producer deliberately never issues makes the MMA warp's
+    bounded wait run out; the kernel reports it and exits cleanly."""
+    w = small("tiny", 512, 512, 256)
+    inp = synth.make_inputs(w, DEV)
+    plan = api.Plan(w.M, w.N, w.K, w.program)
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, inp.A, inp.B, out, bias=inp.bias, timeout_ms=50,
+                    debug_flags=native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD)
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == native.GEMM_EPI_ERR_TIMEOUT
+    # The context still works: a normal run afterwards is correct.
+    api.run_program(plan, inp.A, inp.B, out, bias=inp.bias)
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    compare_rows(w, inp, out)
+
+
+def test_graph_capture_replay_matches_eager():
+    w = small("fp8", 512, 768, 256)
+    inp = synth.make_inputs(w, DEV)
+    plan = api.Plan(w.M, w.N, w.K, w.program)
+    eager = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, inp.A, inp.B, eager, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias)
+    torch.cuda.synchronize()
+    out = api.allocate_outputs(plan, DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
+                            bias=inp.bias)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.C.view(torch.int16), eager.C.view(torch.int16))
+    assert torch.equal(out.C8, eager.C8)
+    assert out.amax.item() == eager.amax.item()
+
+
+# ------------------------------------------------------------ full-size workloads
+
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity(name):
+    w = W[name]
+    inp = synth.make_inputs(w, DEV)
+    plan, out = run_cuda(w, inp)
+    rng = np.random.default_rng(w.index)
+    nrows = 96 if w.M > 128 else w.M
+    rows = np.unique(np.concatenate([rng.choice(w.M, nrows, replace=False), [0, w.M - 1]]))
+    p = oracle_problem(w, inp)
+    ref = compare_rows(w, inp, out, rows=rows, oracle_p=p)
+    ncols = 24 if w.n_out > 64 else w.n_out
+    cols = np.unique(np.concatenate([rng.choice(w.n_out, ncols, replace=False), [0, w.n_out - 1]]))
+    compare_cols(w, inp, out, cols, oracle_p=p)
+    prog = [op.partition(":")[0] for op in w.program]
+    # Invariants over the whole output.
+    if "amax" in prog:
+        amax = float(out.amax.item())
+        cmax = out.C.float().abs().max().item()
+        assert oracle.to_bf16_bits([amax])[0] == oracle.to_bf16_bits([cmax])[0]
+        assert amax >= ref["amax"] * (1 - 2 ** -20)
+    if "row_rms" in prog:
+        c = out.C.float()
+        r = torch.rsqrt(c.pow(2).mean(1, dtype=torch.float64) + 1e-6).float()
+        torch.testing.assert_close(out.row_out, r, rtol=1e-5, atol=0)
+    if "col_sum" in prog:
+        c = out.C.double()
+        s = c.sum(0)
+        bound = 2.0 ** -8 * c.abs().sum(0) + 1e-6
+        assert torch.all((out.col_out.double() - s).abs() <= bound)
