@@ -103,6 +103,11 @@ struct EpiOpDev {
 
 struct KernelParams {
   int32_t M, N, K, n_out;
+  // Output widths the TMA stores cover: n_out rounded down to whole 16-byte
+  // groups (8 bf16 / 16 e4m3 columns).  The tensor unit clips a box at the
+  // tensor edge in 16-byte groups, so the few columns of a ragged last group
+  // are written with plain stores instead.
+  int32_t n_al, n_al8;
   int32_t num_m_tiles, num_n_tiles, num_tiles, num_k_blocks;
   int32_t group_m;
   int32_t b_kn;  // 1: B stored K x N (MN-major operand)
@@ -118,6 +123,9 @@ struct KernelParams {
   float* amax;
   float* row_out;
   float* col_out;
+  uint16_t* c;   // bf16 output (ragged-tail stores)
+  uint8_t* c8;   // e4m3 output (ragged-tail stores)
+  int64_t ldc, ldc8;
   uint32_t* status;       // workspace: [0] error bits, [1] where, [2] block
   uint32_t* row_counter;  // workspace: one arrival counter per M tile
   uint64_t timeout_ns;
@@ -607,6 +615,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 w.w = ptx::pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
                 *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
               }
+              if (col0 + 32 > p.n_al && row_ok) {  // ragged last 16-byte group
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int n = col0 + j;
+                  if (n >= p.n_al && n < p.n_out)
+                    p.c[static_cast<int64_t>(m) * p.ldc + n] =
+                        static_cast<uint16_t>(ptx::pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
+                }
+              }
               break;
             }
             case GEMM_EPI_OP_STORE_E4M3: {
@@ -624,6 +641,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 2) & 1)) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
+              }
+              if (col0 + 32 > p.n_al8 && row_ok) {  // ragged last 16-byte group
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int n = col0 + j;
+                  if (n >= p.n_al8 && n < p.n_out)
+                    p.c8[static_cast<int64_t>(m) * p.ldc8 + n] =
+                        static_cast<uint8_t>(ptx::pack_e4m3x2(v[j] * s, 0.0f) & 0xFFu);
+                }
               }
               break;
             }
@@ -655,10 +681,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             if (flags & (F_STORE | F_E8)) {
-              if (slab_ok && col0 < p.n_out) {
-                if (flags & F_STORE)
+              if (slab_ok) {
+                if ((flags & F_STORE) && col0 < p.n_al)
                   ptx::tma_store_2d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0);
-                if (flags & F_E8)
+                if ((flags & F_E8) && col0 < p.n_al8)
                   ptx::tma_store_2d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0);
               }
               ptx::bulk_commit_group();

@@ -201,6 +201,8 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 
   // Strides: bounds first, then the 16-byte TMA rule.
   const bool kn = d.b_layout == GEMM_EPI_B_KN;
+  if (d.K % 8)  // the K tail of a TMA box is clipped in 16-byte groups
+    return fail(GEMM_EPI_ERR_MISALIGNED, "K must be a multiple of 8 (got %lld)", static_cast<long long>(d.K));
   if (d.K > 0) {  // A and B are not read when K == 0
     if (d.lda < d.K) return fail(GEMM_EPI_ERR_INVALID_VALUE, "lda < K");
     if (d.ldb < (kn ? d.N : d.K) || d.ldb <= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldb too small");
@@ -243,6 +245,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.N = static_cast<int32_t>(d.N);
   k.K = static_cast<int32_t>(d.K);
   k.n_out = static_cast<int32_t>(P.n_out);
+  k.n_al = static_cast<int32_t>(P.n_out / 8 * 8);
+  k.n_al8 = static_cast<int32_t>(P.n_out / 16 * 16);
   k.num_m_tiles = static_cast<int32_t>(P.num_m_tiles);
   k.num_n_tiles = static_cast<int32_t>(P.num_n_tiles);
   k.num_tiles = static_cast<int32_t>(P.num_m_tiles * P.num_n_tiles);
@@ -266,6 +270,10 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.amax = a.amax;
   k.row_out = a.row_out;
   k.col_out = a.col_out;
+  k.c = static_cast<uint16_t*>(a.C);
+  k.c8 = static_cast<uint8_t*>(a.C8);
+  k.ldc = d.ldc;
+  k.ldc8 = d.ldc8;
   k.status = static_cast<uint32_t*>(a.workspace);
   k.row_counter = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + WS_HEADER);
   k.timeout_ns = static_cast<uint64_t>(a.timeout_ms ? a.timeout_ms : DEFAULT_TIMEOUT_MS) * 1000000ull;
@@ -290,13 +298,13 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
     if (s) return s;
   }
-  if (P.flags & ge::F_STORE) {
-    s = make_map(&L.tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, P.n_out, d.M, d.ldc * 2, ge::CHUNK, 32,
+  if ((P.flags & ge::F_STORE) && k.n_al > 0) {
+    s = make_map(&L.tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, k.n_al, d.M, d.ldc * 2, ge::CHUNK, 32,
                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
     if (s) return s;
   }
-  if (P.flags & ge::F_E8) {
-    s = make_map(&L.tc8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.C8, P.n_out, d.M, d.ldc8, ge::CHUNK, 32,
+  if ((P.flags & ge::F_E8) && k.n_al8 > 0) {
+    s = make_map(&L.tc8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.C8, k.n_al8, d.M, d.ldc8, ge::CHUNK, 32,
                  CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C8");
     if (s) return s;
   }

@@ -54,8 +54,14 @@
  *  - row_scale: fp32, M values.  amax: 1 fp32.  row_out: M fp32.
  *    col_out: N_out fp32.
  *  - TMA needs every base pointer 16-byte aligned and every row stride a
- *    multiple of 16 bytes (8 bf16 elements, 16 e4m3 bytes); anything else is
- *    GEMM_EPI_ERR_MISALIGNED.
+ *    multiple of 16 bytes (8 bf16 elements, 16 e4m3 bytes); K must be a
+ *    multiple of 8 (operand rows are read in whole 16-byte groups, so a
+ *    ragged K tail would read the row padding); anything else is
+ *    GEMM_EPI_ERR_MISALIGNED.  N and M need no alignment: outputs are written
+ *    exactly within [0, M) x [0, N_out).  Inputs whose logical row width is
+ *    not a multiple of 16 bytes (B with N % 8 != 0, residual / preact with
+ *    N_out % 8 != 0) may have the rest of their last 16-byte group read; those
+ *    values never reach an output.
  *
  * Errors
  *  - create / run return synchronous validation errors and never launch
@@ -129,7 +135,7 @@ typedef struct gemm_epi_op {
 #define GEMM_EPI_MAX_OPS 16
 
 typedef struct gemm_epi_desc {
-    int64_t M, N, K;          /* GEMM sizes; M, N >= 0, K >= 0 (K == 0: acc = 0) */
+    int64_t M, N, K;          /* GEMM sizes; M, N >= 0; K >= 0, K % 8 == 0 (K == 0: acc = 0) */
     int64_t lda, ldb;         /* row strides of A and B, elements */
     int64_t ldc;              /* row stride of C (bf16 elements); used with STORE_BF16 */
     int64_t ldc8;             /* row stride of C8 (bytes); used with STORE_E4M3 */

@@ -96,6 +96,7 @@ def test_create_accepts_programs(lib, program):
     (dict(layout=7), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(lda=64), N.GEMM_EPI_ERR_INVALID_VALUE),          # lda < K
     (dict(lda=132), N.GEMM_EPI_ERR_MISALIGNED),            # not a multiple of 8
+    (dict(K=12, lda=16), N.GEMM_EPI_ERR_MISALIGNED),       # K tail inside a 16-byte group
     (dict(ldb=516), N.GEMM_EPI_ERR_MISALIGNED),
     (dict(ldc=500), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(ldc=516), N.GEMM_EPI_ERR_MISALIGNED),

@@ -38,7 +38,7 @@ SMALL_SHAPES = [
     ("tiny", 64, 64, 128),          # the tiny workload itself (one partial tile)
     ("tiny", 300, 600, 200),        # 3 x 3 tiles, ragged M, N and K tails
     ("swiglu", 260, 1040, 136),     # pair op, 5 N tiles with a 16-column tail
-    ("fp8", 257, 520, 264),         # FP8 store + AMAX, K tail of 8
+    ("fp8", 257, 528, 264),         # FP8 store + AMAX, 16-column N tail, K tail of 8
     ("downproj", 384, 1000, 328),   # residual + row RMS across 4 N tiles
     ("backward", 200, 776, 192),    # B stored N x K, gelu' + column sums
 ]
@@ -54,14 +54,26 @@ def test_small_full_compare(name, M, N, K):
         compare_cols(w, inp, out, list(range(w.n_out)))
 
 
+def unfused_oracle(w, inp):
+    """The unfused baseline's own definition: the bare GEMM rounded to bf16,
+    then the epilogue program applied to that stored tensor (written as the
+    oracle's GEMM of the stored tensor with an exact bf16 identity)."""
+    p = oracle_problem(w, inp)
+    stored = oracle.Problem(p.A, p.B, ["store_bf16"], b_is_nk=p.b_is_nk).rows()["c_bf16"]
+    eye = oracle.to_bf16_bits(np.eye(w.N))
+    p.A, p.B, p.b_is_nk = stored, eye, False
+    return p
+
+
 @pytest.mark.parametrize("name,M,N,K", SMALL_SHAPES[1:])
 def test_small_unfused_baseline(name, M, N, K):
     w = small(name, M, N, K)
     inp = synth.make_inputs(w, DEV)
     plan, out = run_cuda(w, inp, unfused=True)
-    compare_rows(w, inp, out)
+    p = unfused_oracle(w, inp)
+    compare_rows(w, inp, out, oracle_p=p)
     if out.col_out is not None:
-        compare_cols(w, inp, out, list(range(w.n_out)))
+        compare_cols(w, inp, out, list(range(w.n_out)), oracle_p=p)
 
 
 @pytest.mark.parametrize("program,layout", [
@@ -169,24 +181,31 @@ def test_empty_problem_clears_reductions():
     assert out.amax.item() == 0.0 and torch.all(out.col_out == 0)
 
 
-def test_strided_operands_and_guard_bands():
-    """Row strides larger than the logical width; sentinels beyond every
-    declared extent must survive."""
-    M, N, K = 200, 300, 136
-    lda, ldb, ldc = K + 24, N + 20, N + 36
+@pytest.mark.parametrize("N", [300, 333, 7])
+def test_strided_operands_and_guard_bands(N):
+    """Row strides larger than the logical width and output widths that end
+    inside a 16-byte group; sentinels beyond every declared extent survive."""
+    M, K = 200, 136
+    lda, ldb = K + 24, (N + 7) // 8 * 8 + 16
+    ldc, ldc8 = (N + 7) // 8 * 8 + 32, (N + 15) // 16 * 16 + 32
     g = torch.Generator(device=DEV).manual_seed(3)
     Abuf = torch.randn(M, lda, generator=g, device=DEV).to(torch.bfloat16)
     Bbuf = torch.randn(K, ldb, generator=g, device=DEV).to(torch.bfloat16)
     Cbuf = torch.full((M + 3, ldc), 12345.0, device=DEV).to(torch.bfloat16)
+    C8buf = torch.full((M + 3, ldc8), 0x5A, dtype=torch.uint8, device=DEV)
     sentinel = Cbuf[0, 0].clone()
-    plan = api.Plan(M, N, K, ["gelu_tanh", "store_bf16"], lda=lda, ldb=ldb, ldc=ldc)
+    prog = ["gelu_tanh", "store_bf16", "store_e4m3"]
+    plan = api.Plan(M, N, K, prog, lda=lda, ldb=ldb, ldc=ldc, ldc8=ldc8)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
-    plan.run(Abuf, Bbuf, C=Cbuf, workspace=ws)
+    plan.run(Abuf, Bbuf, C=Cbuf, C8=C8buf, fp8_scale=8.0, workspace=ws)
     torch.cuda.synchronize()
     assert plan.query_status(ws) == 0
     assert torch.all(Cbuf[:M, N:] == sentinel) and torch.all(Cbuf[M:] == sentinel)
-    ref = oracle.Problem(bits(Abuf[:, :K]), bits(Bbuf[:, :N]), ["gelu_tanh", "store_bf16"]).rows()
+    assert torch.all(C8buf[:M, N:] == 0x5A) and torch.all(C8buf[M:] == 0x5A)
+    ref = oracle.Problem(bits(Abuf[:, :K]), bits(Bbuf[:, :N]), prog, fp8_scale=8.0).rows()
     check_bf16(bits(Cbuf[:M, :N]), ref["y"])
+    from parity import check_e4m3
+    check_e4m3(C8buf[:M, :N].cpu().numpy(), ref["c_e4m3"], ref["y"] * 8.0)
 
 
 def test_misaligned_and_missing_buffers_rejected():
