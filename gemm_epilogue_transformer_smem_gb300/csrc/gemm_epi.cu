@@ -51,10 +51,18 @@ constexpr uint32_t DEFAULT_TIMEOUT_MS = 2000;
 struct DeviceState {
   bool ready = false;
   int cc_major = 0, cc_minor = 0, sms = 0;
+  void* no_alloc_scratch = nullptr;  // device address of g_no_alloc_scratch
 };
 
 std::mutex g_mu;
 DeviceState g_dev[128];
+
+// Scratch of gemm_epi_run_no_alloc: the status words and row counters that
+// gemm_epi_run keeps in the caller's workspace.  Every device that loads the
+// library holds this array until the process exits.  On the host its name is
+// only a stand-in; the kernel gets the address cudaGetSymbolAddress returns
+// for the current device.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[GEMM_EPI_NO_ALLOC_SCRATCH_BYTES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 gemm_epi_status device_state(DeviceState** out, int* dev_out) {
@@ -496,6 +504,48 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
     if (e != cudaSuccess) return cuda_fail(e, "launch of the row finalize kernel");
   }
   return GEMM_EPI_OK;
+}
+
+// Same launch as gemm_epi_run with the workspace replaced by the static
+// scratch above.  The first call on a device looks up the scratch's address
+// on that device (no allocation), so make it before any stream capture.
+// Calls share the scratch and clear it on their stream before the kernel:
+// calls whose kernels overlap on the GPU race on it.
+gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args* args, void* stream) {
+  g_last_error.clear();
+  if (!h || !args) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and args must not be NULL");
+  DeviceState* dev = nullptr;
+  int dev_id = 0;
+  gemm_epi_status s = device_state(&dev, &dev_id);
+  if (s) return s;
+  if (h->ws_bytes > GEMM_EPI_NO_ALLOC_SCRATCH_BYTES)
+    return fail(GEMM_EPI_ERR_WORKSPACE,
+                "this plan needs %zu bytes of scratch; the built-in scratch of gemm_epi_run_no_alloc "
+                "holds %d (M is limited to %d rows)",
+                h->ws_bytes, GEMM_EPI_NO_ALLOC_SCRATCH_BYTES,
+                static_cast<int>((GEMM_EPI_NO_ALLOC_SCRATCH_BYTES - WS_HEADER) / 4 * ge::BLOCK_M));
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!dev->no_alloc_scratch) {
+      cudaError_t e = cudaGetSymbolAddress(&dev->no_alloc_scratch, g_no_alloc_scratch);
+      if (e != cudaSuccess) {
+        dev->no_alloc_scratch = nullptr;
+        return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+      }
+    }
+    scratch = dev->no_alloc_scratch;
+  }
+  gemm_epi_args a = *args;
+  a.workspace = scratch;
+  a.workspace_bytes = GEMM_EPI_NO_ALLOC_SCRATCH_BYTES;
+  if ((s = check_args(*h, a))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = clear_outputs(*h, a, st))) return s;
+  if (h->d.M == 0 || h->n_out == 0) return GEMM_EPI_OK;
+  Launch L;
+  if ((s = prepare(*h, a, *dev, L))) return s;
+  return launch_fused(L, st);
 }
 
 gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void* workspace, void* stream) {

@@ -48,6 +48,7 @@ GEMM_EPI_OP_COL_SUM = 14
 
 GEMM_EPI_MAX_OPS = 16
 GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1
+GEMM_EPI_NO_ALLOC_SCRATCH_BYTES = 65536
 
 
 class gemm_epi_op(ctypes.Structure):
@@ -88,6 +89,7 @@ SIGNATURES = [
     ("gemm_epi_run", ctypes.c_int, [gemm_epi_handle, ctypes.POINTER(gemm_epi_args), ctypes.c_void_p]),
     ("gemm_epi_run_unfused", ctypes.c_int,
      [gemm_epi_handle, ctypes.POINTER(gemm_epi_args), ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
+    ("gemm_epi_run_no_alloc", ctypes.c_int, [gemm_epi_handle, ctypes.POINTER(gemm_epi_args), ctypes.c_void_p]),
     ("gemm_epi_query_status", ctypes.c_int, [gemm_epi_handle, ctypes.c_void_p, ctypes.c_void_p]),
     ("gemm_epi_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("gemm_epi_last_error", ctypes.c_char_p, []),

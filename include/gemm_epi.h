@@ -197,6 +197,31 @@ gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args *args, void 
 gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args *args,
                                      void *scratch, int64_t ld_scratch, void *stream);
 
+/* Allocation-free variant of gemm_epi_run.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * code running inside a host framework or plugin interface that hands it
+ * only input and output pointers and owns every other allocation, or a
+ * latency-critical loop that must not pay for cudaMalloc's implicit device
+ * synchronisation -- and so have no way to supply a workspace.
+ *  - Same arguments and semantics as gemm_epi_run; args->workspace and
+ *    args->workspace_bytes are ignored.  Nothing is allocated: no cudaMalloc,
+ *    cudaFree or allocating library routine is called.
+ *  - The scratch (status words and per-row-tile counters) is one static
+ *    device array of GEMM_EPI_NO_ALLOC_SCRATCH_BYTES bytes inside the
+ *    library; every GPU that loads the library keeps it until the process
+ *    exits.  Plans whose gemm_epi_workspace_size exceeds it (M above
+ *    2,088,960 rows) are rejected with GEMM_EPI_ERR_WORKSPACE.
+ *  - The first call on a device looks up the array's address on that device
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the array and clear it on their stream before the
+ *    kernel; calls whose kernels overlap on the GPU (several streams, several
+ *    host threads) race on it and must be serialised by the caller.
+ *  - A timed-out in-kernel wait is recorded in that array and is not
+ *    reported back; use gemm_epi_run with a workspace and
+ *    gemm_epi_query_status when the status is needed. */
+#define GEMM_EPI_NO_ALLOC_SCRATCH_BYTES 65536
+gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
+
 /* Synchronises `stream`, then reads the status word the last run on that
  * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
 gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
