@@ -14,9 +14,17 @@
 //               box, or four MN-major 64x64 boxes) into a STAGES-deep ring of
 //               128B-swizzled shared-memory stages, mbarrier transaction counts.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators),
-//               then one lane issues tcgen05.mma (M=128, N=256, K=16) and
-//               commits each stage back to the producer and each finished
+//               then one lane issues tcgen05.mma (N=256, K=16) and commits
+//               each stage back to the producer and each finished
 //               accumulator to the epilogue.
+// Two main-loop shapes share the code (template parameter CG):
+//   CG = 1  one CTA per 128 x 256 tile, M = 128 MMAs, 4 stages of 48 KB.
+//   CG = 2  a cluster of two CTAs per 256 x 256 tile: each CTA stages its
+//           128 rows of A and its 128 columns of B (6 stages of 32 KB), the
+//           even CTA issues tcgen05.mma.cta_group::2 (M = 256) for the pair
+//           and multicasts its commits to both CTAs; each CTA's epilogue
+//           drains the 128 x 256 accumulator in its own TMEM.  Each SM then
+//           stages a third less operand data per FLOP than with CG = 1.
 //   warps 2..5  epilogue: warp w drains TMEM lanes 32*(w%4).. with
 //               tcgen05.ld (thread = row, register = column), runs the op
 //               program in registers, stages bf16 / e4m3 results in swizzled
@@ -42,7 +50,6 @@ constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 256;
 constexpr int BLOCK_K = 64;  // 64 bf16 = 128 bytes = one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int CHUNK = 32;     // output columns per epilogue step
@@ -51,28 +58,35 @@ constexpr int E8_BUFS = 2;    // e4m3 staging buffers per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;
 
 constexpr uint32_t A_STAGE_BYTES = BLOCK_M * BLOCK_K * 2;
-constexpr uint32_t B_STAGE_BYTES = BLOCK_N * BLOCK_K * 2;
 constexpr uint32_t B_MN_BOX_BYTES = 64 * BLOCK_K * 2;  // one 64-column MN-major box
 constexpr uint32_t EPI_BUF_BYTES = 32 * CHUNK * 2;     // 32 rows x 64 bytes
 constexpr uint32_t E8_BUF_BYTES = 32 * CHUNK;          // 32 rows x 32 bytes
+constexpr uint64_t DRAIN_LIMIT_NS = 20000000ull;       // bound of the abort-path drains
 
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
-constexpr uint32_t OFF_E8 = OFF_EPI + NUM_EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-constexpr uint32_t OFF_BAR = OFF_E8 + NUM_EPI_WARPS * E8_BUFS * E8_BUF_BYTES;
-constexpr uint32_t BAR_FULL = 0;
-constexpr uint32_t BAR_EMPTY = BAR_FULL + STAGES;
-constexpr uint32_t BAR_TFULL = BAR_EMPTY + STAGES;
-constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 2;
-constexpr uint32_t BAR_AUX = BAR_TEMPTY + 2;
-constexpr uint32_t BAR_DRAIN = BAR_AUX + NUM_EPI_WARPS * EPI_BUFS;
-constexpr uint32_t NUM_BARS = BAR_DRAIN + 1;
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_USED = OFF_MISC + 16;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // room to align the base to 1 KB
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
-static_assert(OFF_EPI % 1024 == 0 && OFF_E8 % 1024 == 0, "staging buffers must stay aligned");
+// Shared-memory map of one CTA when CG CTAs share a tile.
+template <int CG>
+struct Smem {
+  static constexpr int STAGES = CG == 1 ? 4 : 6;
+  static constexpr int B_COLS = BLOCK_N / CG;  // B columns (N) this CTA stages
+  static constexpr uint32_t B_STAGE_BYTES = B_COLS * BLOCK_K * 2;
+  static constexpr uint32_t OFF_A = 0;
+  static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+  static constexpr uint32_t OFF_E8 = OFF_EPI + NUM_EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_E8 + NUM_EPI_WARPS * E8_BUFS * E8_BUF_BYTES;
+  static constexpr uint32_t BAR_FULL = 0;
+  static constexpr uint32_t BAR_EMPTY = BAR_FULL + STAGES;
+  static constexpr uint32_t BAR_TFULL = BAR_EMPTY + STAGES;
+  static constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 2;
+  static constexpr uint32_t BAR_AUX = BAR_TEMPTY + 2;
+  static constexpr uint32_t BAR_DRAIN = BAR_AUX + NUM_EPI_WARPS * EPI_BUFS;
+  static constexpr uint32_t NUM_BARS = BAR_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;  // + room to align the base to 1 KB
+  static_assert(BYTES <= 232448, "shared memory budget of one CTA exceeded");
+  static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_E8 % 1024 == 0,
+                "operand and staging buffers must stay 1 KB aligned");
+};
 
 // Program flags derived on the host.
 enum : uint32_t {
@@ -127,7 +141,7 @@ struct KernelParams {
   uint8_t* c8;   // e4m3 output (ragged-tail stores)
   int64_t ldc, ldc8;
   uint32_t* status;       // workspace: [0] error bits, [1] where, [2] block
-  uint32_t* row_counter;  // workspace: one arrival counter per M tile
+  uint32_t* row_counter;  // workspace: one arrival counter per 128-row block
   uint64_t timeout_ns;
   uint32_t debug_flags;
   EpiOpDev ops[GEMM_EPI_MAX_OPS];
@@ -145,6 +159,7 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& m
   nb = r / gsz;
 }
 
+template <int CG>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        const KernelParams& p, uint32_t where) {
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -156,6 +171,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile u
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       *abort_flag = 1u;
+      if (CG == 2) {  // the peer CTA stops waiting on this one too
+        const uint32_t mine = ptx::smem_addr(const_cast<uint32_t*>(abort_flag));
+        ptx::st_shared_cluster_u32(ptx::mapa_shared(mine, ptx::cluster_ctarank() ^ 1u), 1u);
+      }
       if (atomicOr(p.status, 1u) == 0u) {
         p.status[1] = where;
         p.status[2] = blockIdx.x;
@@ -167,10 +186,11 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile u
 }
 
 // Bounded wait for the phase of parity `parity` of mbarrier `bar`.
+template <int CG>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          const KernelParams& p, uint32_t where) {
   if (ptx::mbar_test(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, p, where);
+  return wait_slow<CG>(bar, parity, abort_flag, p, where);
 }
 
 // Short bounded wait used while draining after an abort (no flag check).
@@ -315,6 +335,7 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 
 // ------------------------------------------------------------------ kernel
 
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tm_a,
                                const __grid_constant__ CUtensorMap tm_b,
@@ -322,17 +343,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                const __grid_constant__ CUtensorMap tm_c8,
                                const __grid_constant__ CUtensorMap tm_aux,
                                const __grid_constant__ KernelParams p) {
+  using L = Smem<CG>;
+  constexpr int STAGES = L::STAGES;
+  constexpr int TILE_M = BLOCK_M * CG;  // rows of one tile (the whole CTA group)
+  constexpr uint32_t BAR_FULL = L::BAR_FULL, BAR_EMPTY = L::BAR_EMPTY, BAR_TFULL = L::BAR_TFULL,
+                     BAR_TEMPTY = L::BAR_TEMPTY, BAR_AUX = L::BAR_AUX, BAR_DRAIN = L::BAR_DRAIN;
   extern __shared__ uint8_t smem_raw[];
+  // Same offset in both CTAs of a pair: the pair MMA addresses the peer's
+  // operands and accumulator by this CTA's offsets.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
-  const uint32_t bar0 = sbase + OFF_BAR;
+  const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;  // CTA within the pair
+  const int group = blockIdx.x / CG;                             // tile-walker index
+  const int num_groups = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < STAGES; ++s) {
@@ -341,7 +372,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (uint32_t b = 0; b < 2; ++b) {
       ptx::mbar_init(bar(BAR_TFULL + b), 1);
-      ptx::mbar_init(bar(BAR_TEMPTY + b), NUM_EPI_WARPS);
+      ptx::mbar_init(bar(BAR_TEMPTY + b), NUM_EPI_WARPS * CG);  // every epilogue warp of the group
     }
     for (uint32_t i = 0; i < NUM_EPI_WARPS * EPI_BUFS; ++i) ptx::mbar_init(bar(BAR_AUX + i), 1);
     ptx::mbar_init(bar(BAR_DRAIN), 1);
@@ -349,15 +380,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(sbase + OFF_MISC, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (CG == 2) {
+      ptx::tmem_alloc_cg2(sbase + L::OFF_MISC, TMEM_COLS);
+      ptx::tmem_relinquish_cg2();
+    } else {
+      ptx::tmem_alloc(sbase + L::OFF_MISC, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && p.num_k_blocks > 0) {
     ptx::tma_prefetch_desc(&tm_a);
     ptx::tma_prefetch_desc(&tm_b);
   }
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  if (CG == 2)
+    ptx::cluster_sync();  // the peer's barriers are initialised before anyone signals them
+  else
+    __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = misc[0];
 
@@ -367,29 +406,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-stage bits, for the abort drain
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = group; ok && t < p.num_tiles; t += num_groups) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
+        const int a_row = mb * TILE_M + rank * BLOCK_M;
+        const int b_col = nb * BLOCK_N + rank * L::B_COLS;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!wait_bar(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
+          if (!wait_bar<CG>(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
           const bool skip = (p.debug_flags & GEMM_EPI_DEBUG_SKIP_FIRST_LOAD) && blockIdx.x == 0 &&
-                            t == static_cast<int>(blockIdx.x) && kb == 0;
+                            t == group && kb == 0;
           if (!skip) {
             const uint32_t fb = bar(BAR_FULL + stage);
-            ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-            const uint32_t sa = sbase + OFF_A + stage * A_STAGE_BYTES;
-            const uint32_t sb = sbase + OFF_B + stage * B_STAGE_BYTES;
-            ptx::tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, mb * BLOCK_M);
-            if (p.b_kn) {
+            const uint32_t sa = sbase + L::OFF_A + stage * A_STAGE_BYTES;
+            const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
+            if (CG == 1) {
+              ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + L::B_STAGE_BYTES);
+              ptx::tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, a_row);
+              if (p.b_kn) {
 #pragma unroll
-              for (int j = 0; j < BLOCK_N / 64; ++j)
-                ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, &tm_b, fb, nb * BLOCK_N + j * 64,
-                                 kb * BLOCK_K);
+                for (int j = 0; j < L::B_COLS / 64; ++j)
+                  ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, &tm_b, fb, b_col + j * 64, kb * BLOCK_K);
+              } else {
+                ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, b_col);
+              }
             } else {
-              ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, nb * BLOCK_N);
+              // Both CTAs' halves complete on the even CTA's full barrier,
+              // which expects the bytes of the whole pair.
+              const uint32_t fb0 = ptx::mapa_shared(fb, 0);
+              if (rank == 0) ptx::mbar_arrive_expect_tx(fb, 2u * (A_STAGE_BYTES + L::B_STAGE_BYTES));
+              ptx::tma_load_2d_cg2(sa, &tm_a, fb0, kb * BLOCK_K, a_row);
+              if (p.b_kn) {
+#pragma unroll
+                for (int j = 0; j < L::B_COLS / 64; ++j)
+                  ptx::tma_load_2d_cg2(sb + j * B_MN_BOX_BYTES, &tm_b, fb0, b_col + j * 64, kb * BLOCK_K);
+              } else {
+                ptx::tma_load_2d_cg2(sb, &tm_b, fb0, kb * BLOCK_K, b_col);
+              }
             }
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -402,58 +457,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && rank == 0) {
+        // Loads still in flight land before the CTA exits.  (The odd CTA of a
+        // pair cannot observe its loads, which complete on the even CTA's
+        // barrier; the abort path waits out a fixed delay at the end.)
         for (uint32_t s = 0; s < STAGES; ++s)
-          if (issued & (1u << s)) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, p.timeout_ns);
+          if (issued & (1u << s)) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, DRAIN_LIMIT_NS);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {  // the even CTA issues for the whole group
       uint32_t stage = 0, phase = 0;
       bool ok = true, any_mma = false;
       int local = 0;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+      for (int t = group; ok && t < p.num_tiles; t += num_groups, ++local) {
         const uint32_t buf = local & 1, use = local >> 1;
-        if (!wait_bar(bar(BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p, W_MMA_TMEM_EMPTY)) {
+        if (!wait_bar<CG>(bar(BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p, W_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after_sync();
         if (p.num_k_blocks == 0) {
-          ptx::mbar_arrive(bar(BAR_TFULL + buf));
+          if (CG == 1) {
+            ptx::mbar_arrive(bar(BAR_TFULL + buf));
+          } else {
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(BAR_TFULL + buf), 0));
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(BAR_TFULL + buf), 1));
+          }
           continue;
         }
         const uint32_t d_tmem = tmem_base + buf * BLOCK_N;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!wait_bar(bar(BAR_FULL + stage), phase, abort_flag, p, W_MMA_FULL)) {
+          if (!wait_bar<CG>(bar(BAR_FULL + stage), phase, abort_flag, p, W_MMA_FULL)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after_sync();
-          const uint32_t sa = sbase + OFF_A + stage * A_STAGE_BYTES;
-          const uint32_t sb = sbase + OFF_B + stage * B_STAGE_BYTES;
+          const uint32_t sa = sbase + L::OFF_A + stage * A_STAGE_BYTES;
+          const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
             const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
             const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
                                        : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
-            ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            if (CG == 1)
+              ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
           }
           any_mma = true;
-          ptx::mma_commit(bar(BAR_EMPTY + stage));
+          if (CG == 1)
+            ptx::mma_commit(bar(BAR_EMPTY + stage));
+          else
+            ptx::mma_commit_cg2_multicast(bar(BAR_EMPTY + stage), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(bar(BAR_TFULL + buf));
+        if (CG == 1)
+          ptx::mma_commit(bar(BAR_TFULL + buf));
+        else
+          ptx::mma_commit_cg2_multicast(bar(BAR_TFULL + buf), 0x3);
       }
       if (any_mma) {
         // Every MMA this thread issued is complete before TMEM is released.
-        ptx::mma_commit(bar(BAR_DRAIN));
-        drain_wait(bar(BAR_DRAIN), 0, p.timeout_ns);
+        if (CG == 1)
+          ptx::mma_commit(bar(BAR_DRAIN));
+        else
+          ptx::mma_commit_cg2(bar(BAR_DRAIN));
+        drain_wait(bar(BAR_DRAIN), 0, DRAIN_LIMIT_NS);
       }
     }
   } else {
@@ -465,10 +540,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
     const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
     const uint32_t flags = p.flags;
-    const uint32_t epi0 = sbase + OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
-    const uint32_t e80 = sbase + OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
-    uint8_t* epi0_ptr = smem + OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
-    uint8_t* e80_ptr = smem + OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
+    const uint32_t epi0 = sbase + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
+    const uint32_t e80 = sbase + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
+    uint8_t* epi0_ptr = smem + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
+    uint8_t* e80_ptr = smem + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     const int op_begin = paired ? pair_at + 1 : 0;
     const uint64_t aux_policy = ptx::policy_evict_first();
 
@@ -485,13 +560,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tma_load_2d_hint(epi0 + i * EPI_BUF_BYTES, &tm_aux, b, col, row0, aux_policy);
     };
 
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+    for (int t = group; ok && t < p.num_tiles; t += num_groups, ++local) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int row_in_tile = quad * 32 + lane;
-      const int m = mb * BLOCK_M + row_in_tile;
+      const int blk = mb * CG + static_cast<int>(rank);  // this CTA's 128-row block
+      const int m = blk * BLOCK_M + quad * 32 + lane;
       const bool row_ok = m < p.M;
-      const int slab_row0 = mb * BLOCK_M + quad * 32;
+      const int slab_row0 = blk * BLOCK_M + quad * 32;
       const bool slab_ok = slab_row0 < p.M;
       const int n0 = nb * tile_out_cols;       // first output column of the tile
       const int nacc0 = nb * BLOCK_N;          // first accumulator column
@@ -511,7 +586,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // All lanes wait; the outcome is made warp-uniform so that no lane
       // leaves while the others enter a warp-synchronous step.
       if (!__all_sync(0xffffffffu,
-                      wait_bar(bar(BAR_TFULL + buf), use & 1u, abort_flag, p, W_EPI_TMEM_FULL))) {
+                      wait_bar<CG>(bar(BAR_TFULL + buf), use & 1u, abort_flag, p, W_EPI_TMEM_FULL))) {
         ok = false;
         break;
       }
@@ -555,13 +630,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // The accumulator buffer is free for the next tile's MMAs.
           ptx::tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(BAR_TEMPTY + buf));
+          if (lane == 0) {
+            if (CG == 1)
+              ptx::mbar_arrive(bar(BAR_TEMPTY + buf));
+            else
+              ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(BAR_TEMPTY + buf), 0));
+          }
         }
 
         // ---- auxiliary tile (residual / pre-activation), this thread's row
         float x[32];
         if (flags & F_AUX) {
-          if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_AUX + ew * EPI_BUFS + eb),
+          if (!__all_sync(0xffffffffu, wait_bar<CG>(bar(BAR_AUX + ew * EPI_BUFS + eb),
                                                 (g / EPI_BUFS) & 1u, abort_flag, p, W_EPI_AUX))) {
             ok = false;
             break;
@@ -708,13 +788,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __threadfence();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(p.row_counter + mb, 1u);
+        if (lane == 0) prev = atomicAdd(p.row_counter + blk, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == static_cast<uint32_t>(NUM_EPI_WARPS * p.num_n_tiles - 1)) {
           __threadfence();
           const float inv_n = 1.0f / static_cast<float>(p.n_out);
           for (int r = lane; r < BLOCK_M; r += 32) {
-            const int mm = mb * BLOCK_M + r;
+            const int mm = blk * BLOCK_M + r;
             if (mm < p.M) {
               const float ss = __ldcg(p.row_out + mm);
               p.row_out[mm] = 1.0f / sqrtf(fmaf(ss, inv_n, p.rms_eps));
@@ -729,7 +809,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::bulk_wait_group<0>();
       // Aux loads still in flight after an abort land before the CTA exits.
       for (uint32_t g = aux_done; g < aux_issued; ++g)
-        drain_wait(bar(BAR_AUX + ew * EPI_BUFS + g % EPI_BUFS), (g / EPI_BUFS) & 1u, p.timeout_ns);
+        drain_wait(bar(BAR_AUX + ew * EPI_BUFS + g % EPI_BUFS), (g / EPI_BUFS) & 1u, DRAIN_LIMIT_NS);
     }
     if (flags & F_AMAX) {
 #pragma unroll
@@ -738,11 +818,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  if (threadIdx.x == 0 && *abort_flag) {
+    // After an abort, copies this CTA cannot observe (the odd CTA's operand
+    // loads) get a fixed 200 us to land before shared memory is released.
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  __syncwarp();  // role branches reconverge before the warp-aligned barrier
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  if (CG == 2)
+    ptx::cluster_sync();  // no CTA of the pair releases TMEM or smem the other still uses
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CG == 2)
+      ptx::tmem_dealloc_cg2(tmem_base, TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

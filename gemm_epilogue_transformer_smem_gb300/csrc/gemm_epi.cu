@@ -51,6 +51,7 @@ constexpr uint32_t DEFAULT_TIMEOUT_MS = 2000;
 struct DeviceState {
   bool ready = false;
   int cc_major = 0, cc_minor = 0, sms = 0;
+  int pair_clusters = 0;  // CTA pairs of the 2-SM kernel that fit on the GPU at once
   void* no_alloc_scratch = nullptr;  // device address of g_no_alloc_scratch
 };
 
@@ -78,9 +79,30 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
         (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if (d.cc_major == 10 && d.cc_minor == 3) {
-      e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, ge::SMEM_BYTES);
+      e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<1>::BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel<2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<2>::BYTES);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+      // How many CTA pairs the GPU holds at once (a persistent grid larger
+      // than that would leave pairs waiting for others to finish).
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof cfg);
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * d.sms, 1, 1);
+      cfg.blockDim = dim3(ge::NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = ge::Smem<2>::BYTES;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, ge::fused_gemm_epilogue_kernel<2>, &cfg);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+      d.pair_clusters = clusters;
     }
     if (!g_encode) {
       void* fn = nullptr;
@@ -232,7 +254,10 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   P.num_m_tiles = (d.M + ge::BLOCK_M - 1) / ge::BLOCK_M;
   P.num_n_tiles = (d.N + ge::BLOCK_N - 1) / ge::BLOCK_N;
   if (P.num_m_tiles * P.num_n_tiles > LIM) return fail(GEMM_EPI_ERR_INVALID_VALUE, "too many tiles");
-  P.ws_bytes = WS_HEADER + ((static_cast<size_t>(P.num_m_tiles) * 4 + 255) / 256) * 256;
+  // One row counter per 128-row block, counted in whole 256-row tiles so
+  // both main-loop shapes fit.
+  const size_t row_blocks = static_cast<size_t>((d.M + 2 * ge::BLOCK_M - 1) / (2 * ge::BLOCK_M)) * 2;
+  P.ws_bytes = WS_HEADER + ((row_blocks * 4 + 255) / 256) * 256;
   return GEMM_EPI_OK;
 }
 
@@ -240,7 +265,17 @@ struct Launch {
   CUtensorMap ta, tb, tc, tc8, taux;
   ge::KernelParams kp;
   int grid;
+  int cg;  // CTAs per tile: 1 (128 x 256) or 2 (a CTA pair, 256 x 256)
 };
+
+// 2-SM tiles unless the problem has a single 128-row block (then half of
+// every pair would idle) or a test forces one shape.
+int choose_cta_group(const gemm_epi_plan& P, const gemm_epi_args& a, const DeviceState& dev) {
+  if (a.debug_flags & GEMM_EPI_DEBUG_FORCE_1SM) return 1;
+  if (dev.pair_clusters <= 0) return 1;
+  if (a.debug_flags & GEMM_EPI_DEBUG_FORCE_2SM) return 2;
+  return P.d.M > ge::BLOCK_M ? 2 : 1;
+}
 
 // Fills the kernel parameters and tensor maps of one fused launch.  `c`/`ldc`
 // may differ from the plan's (the unfused baseline stores the bare
@@ -248,6 +283,8 @@ struct Launch {
 gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const DeviceState& dev, Launch& L) {
   const gemm_epi_desc& d = P.d;
   std::memset(&L, 0, sizeof L);
+  L.cg = choose_cta_group(P, a, dev);
+  const int tile_m = ge::BLOCK_M * L.cg;
   ge::KernelParams& k = L.kp;
   k.M = static_cast<int32_t>(d.M);
   k.N = static_cast<int32_t>(d.N);
@@ -255,16 +292,16 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.n_out = static_cast<int32_t>(P.n_out);
   k.n_al = static_cast<int32_t>(P.n_out / 8 * 8);
   k.n_al8 = static_cast<int32_t>(P.n_out / 16 * 16);
-  k.num_m_tiles = static_cast<int32_t>(P.num_m_tiles);
+  k.num_m_tiles = static_cast<int32_t>((d.M + tile_m - 1) / tile_m);
   k.num_n_tiles = static_cast<int32_t>(P.num_n_tiles);
-  k.num_tiles = static_cast<int32_t>(P.num_m_tiles * P.num_n_tiles);
+  k.num_tiles = k.num_m_tiles * k.num_n_tiles;
   k.num_k_blocks = static_cast<int32_t>((d.K + ge::BLOCK_K - 1) / ge::BLOCK_K);
   k.group_m = DEFAULT_GROUP_M;
   k.b_kn = d.b_layout == GEMM_EPI_B_KN ? 1 : 0;
   // Instruction descriptor: D fp32, A and B bf16, A K-major, B K- or
-  // MN-major, N = 256, M = 128.
+  // MN-major, N = 256, M = 128 per CTA of the group.
   k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (k.b_kn ? (1u << 16) : 0u) |
-            (static_cast<uint32_t>(ge::BLOCK_N >> 3) << 17) | (static_cast<uint32_t>(ge::BLOCK_M >> 4) << 24);
+            (static_cast<uint32_t>(ge::BLOCK_N >> 3) << 17) | (static_cast<uint32_t>(tile_m >> 4) << 24);
   k.flags = P.flags;
   k.n_ops = static_cast<int32_t>(P.ops.size());
   k.pair_at = P.pair_at;
@@ -291,7 +328,10 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
     k.ops[i].i0 = P.ops[i].i0;
     k.ops[i].f0 = P.ops[i].f0;
   }
-  L.grid = static_cast<int>(std::min<int64_t>(k.num_tiles, dev.sms));
+  if (L.cg == 2)
+    L.grid = 2 * static_cast<int>(std::min<int64_t>(k.num_tiles, dev.pair_clusters));
+  else
+    L.grid = static_cast<int>(std::min<int64_t>(k.num_tiles, dev.sms));
 
   gemm_epi_status s;
   if (d.K > 0) {
@@ -302,8 +342,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
       s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.N, d.K, d.ldb * 2, 64, ge::BLOCK_K,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
     else
-      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.K, d.N, d.ldb * 2, ge::BLOCK_K, ge::BLOCK_N,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
+      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.K, d.N, d.ldb * 2, ge::BLOCK_K,
+                   ge::BLOCK_N / L.cg, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
     if (s) return s;
   }
   if ((P.flags & ge::F_STORE) && k.n_al > 0) {
@@ -371,9 +411,22 @@ gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(ge::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = ge::SMEM_BYTES;
   cfg.stream = st;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
+  cudaError_t e;
+  if (L.cg == 2) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cfg.dynamicSmemBytes = ge::Smem<2>::BYTES;
+    e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel<2>, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
+  } else {
+    cfg.dynamicSmemBytes = ge::Smem<1>::BYTES;
+    e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel<1>, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
+  }
   return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the fused kernel");
 }
 

@@ -48,6 +48,8 @@ GEMM_EPI_OP_COL_SUM = 14
 
 GEMM_EPI_MAX_OPS = 16
 GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1
+GEMM_EPI_DEBUG_FORCE_1SM = 2
+GEMM_EPI_DEBUG_FORCE_2SM = 4
 GEMM_EPI_NO_ALLOC_SCRATCH_BYTES = 65536
 
 

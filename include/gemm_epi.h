@@ -168,6 +168,11 @@ typedef struct gemm_epi_args {
 /* Test hook: the producer skips the first operand load of the first CTA so
  * that the consumer's bounded wait runs out (nothing is left in flight). */
 #define GEMM_EPI_DEBUG_SKIP_FIRST_LOAD 1u
+/* Test hooks: run the 1-SM main loop (one CTA per 128 x 256 tile) or the
+ * 2-SM one (a CTA pair per 256 x 256 tile) whatever M is.  By default the
+ * 2-SM loop runs when M > 128. */
+#define GEMM_EPI_DEBUG_FORCE_1SM 2u
+#define GEMM_EPI_DEBUG_FORCE_2SM 4u
 
 typedef struct gemm_epi_plan *gemm_epi_handle;
 

@@ -44,11 +44,17 @@ SMALL_SHAPES = [
 ]
 
 
+# The two main-loop shapes: one CTA per 128 x 256 tile, or a CTA pair per
+# 256 x 256 tile (the default whenever M > 128).
+VARIANTS = {"1sm": native.GEMM_EPI_DEBUG_FORCE_1SM, "2sm": native.GEMM_EPI_DEBUG_FORCE_2SM}
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("name,M,N,K", SMALL_SHAPES)
-def test_small_full_compare(name, M, N, K):
+def test_small_full_compare(name, M, N, K, variant):
     w = small(name, M, N, K) if (M, N, K) != (W[name].M, W[name].N, W[name].K) else W[name]
     inp = synth.make_inputs(w, DEV)
-    plan, out = run_cuda(w, inp)
+    plan, out = run_cuda(w, inp, debug_flags=VARIANTS[variant])
     compare_rows(w, inp, out)
     if out.col_out is not None:
         compare_cols(w, inp, out, list(range(w.n_out)))
@@ -76,6 +82,7 @@ def test_small_unfused_baseline(name, M, N, K):
         compare_cols(w, inp, out, list(range(w.n_out)), oracle_p=p)
 
 
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("program,layout", [
     (("store_bf16",), "kn"),
     (("store_bf16",), "nk"),
@@ -87,7 +94,7 @@ def test_small_unfused_baseline(name, M, N, K):
     (("residual", "gelu_tanh", "store_bf16", "store_e4m3", "row_rms_unrounded:1e-5"), "nk"),
     (("gelu_tanh_grad", "amax", "store_bf16", "col_sum", "row_rms"), "kn"),
 ])
-def test_program_variants(program, layout):
+def test_program_variants(program, layout, variant):
     aux = "residual" if "residual" in program else ("preact" if "gelu_tanh_grad" in program else None)
     w = synth.Workload("variant", 11, 200, 512 + 64, 136, layout, program, a_std=0.3, b_std=0.3,
                        bias_std=0.1 if "bias" in program else None, aux=aux, alpha=0.75, fp8_scale=64.0)
@@ -96,7 +103,7 @@ def test_program_variants(program, layout):
     plan = api.Plan(w.M, w.N, w.K, program, b_layout=layout)
     out = api.allocate_outputs(plan, DEV)
     api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias,
-                    row_scale=row_scale, aux=inp.aux)
+                    row_scale=row_scale, aux=inp.aux, debug_flags=VARIANTS[variant])
     torch.cuda.synchronize()
     assert plan.query_status(out.workspace) == 0
     p = oracle_problem(w, inp)
@@ -160,12 +167,14 @@ def test_row_scale_rewrite_identity():
 
 # ------------------------------------------------------------ edge cases
 
-@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 256, 8), (127, 264, 64), (129, 8, 72), (64, 64, 0)])
-def test_edge_shapes(M, N, K):
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 256, 8), (127, 264, 64), (129, 8, 72), (64, 64, 0),
+                                   (300, 520, 0)])
+def test_edge_shapes(M, N, K, variant):
     w = synth.Workload("edge", 12, M, N, K, "kn", ("alpha", "bias", "gelu_tanh", "amax", "store_bf16"),
                        a_std=0.5, b_std=0.5, bias_std=0.1, alpha=1.5)
     inp = synth.make_inputs(w, DEV, seed=99)
-    plan, out = run_cuda(w, inp)
+    plan, out = run_cuda(w, inp, debug_flags=VARIANTS[variant])
     compare_rows(w, inp, out)
 
 
@@ -224,7 +233,8 @@ def test_misaligned_and_missing_buffers_rejected():
     assert e.value.status == native.GEMM_EPI_ERR_WORKSPACE
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_bounded_wait_reports_timeout_and_context_survives(variant):
     """A load the producer deliberately never issues makes the MMA warp's
     bounded wait run out; the kernel reports it and exits cleanly."""
     w = small("tiny", 512, 512, 256)
@@ -232,7 +242,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     plan = api.Plan(w.M, w.N, w.K, w.program)
     out = api.allocate_outputs(plan, DEV)
     api.run_program(plan, inp.A, inp.B, out, bias=inp.bias, timeout_ms=50,
-                    debug_flags=native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD)
+                    debug_flags=native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD | VARIANTS[variant])
     torch.cuda.synchronize()
     assert plan.query_status(out.workspace) == native.GEMM_EPI_ERR_TIMEOUT
     # The context still works: a normal run afterwards is correct.
