@@ -41,7 +41,7 @@
 
 #include <stdint.h>
 
-#include "../../include/gemm_epi.h"
+#include "gemm_epi.h"
 #include "ptx.cuh"
 
 namespace ge {
@@ -54,6 +54,7 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int CHUNK = 32;     // output columns per epilogue step
 constexpr int EPI_BUFS = 3;   // bf16 / aux staging buffers per epilogue warp
+constexpr int AUX_AHEAD = EPI_BUFS - 1;  // aux tiles loaded this many chunks ahead
 constexpr int E8_BUFS = 2;    // e4m3 staging buffers per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;
 
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (flags & F_AUX) {
         if (lane == 0) {
           ptx::bulk_wait_group_read<0>();
-          const int first = min(2, chunks);
+          const int first = min(AUX_AHEAD, chunks);
           for (int c = 0; c < first; ++c) issue_aux(gchunk + c, n0 + c * CHUNK, slab_row0);
           aux_issued = gchunk + first;
         }
@@ -754,8 +755,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
 
-        // ---- stores of this chunk, then the aux load two chunks ahead into
-        // the buffer whose store (chunk g-1) has finished reading it.
+        // ---- stores of this chunk, then the aux load AUX_AHEAD chunks ahead
+        // into the buffer whose store (chunk g-1) has finished reading it.
         if (flags & (F_STORE | F_E8 | F_AUX)) {
           ptx::fence_proxy_async_smem();  // generic smem accesses before async-proxy ones
           __syncwarp();
@@ -770,9 +771,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::bulk_commit_group();
               ptx::bulk_wait_group_read<1>();
             }
-            if ((flags & F_AUX) && c + 2 < chunks) {
-              issue_aux(g + 2, n0 + (c + 2) * CHUNK, slab_row0);
-              aux_issued = g + 3;
+            if ((flags & F_AUX) && c + AUX_AHEAD < chunks) {
+              issue_aux(g + AUX_AHEAD, n0 + (c + AUX_AHEAD) * CHUNK, slab_row0);
+              aux_issued = g + AUX_AHEAD + 1;
             }
           }
         }

@@ -22,7 +22,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/gemm_epi.h"
+#include "gemm_epi.h"
 #include "fused_kernel.cuh"
 #include "unfused_kernel.cuh"
 
