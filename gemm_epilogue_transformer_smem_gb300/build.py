@@ -1,9 +1,11 @@
-"""Compiles the CUDA library (csrc/gemm_epi.cu) for sm_103a into
+"""Compiles the CUDA library (csrc/*.cu) for sm_103a into
 ``_build/libgemm_epi.so`` inside this package.
 
-The cudart runtime is linked statically and the driver's tensor-map encoder is
-looked up at run time, so the library loads on a machine without a GPU
-driver; every compute call then fails with a CUDA error.
+Each translation unit compiles in its own nvcc process, in parallel, then one
+nvcc call links them.  The cudart runtime is linked statically and the
+driver's tensor-map encoder is looked up at run time, so the library loads on
+a machine without a GPU driver; every compute call then fails with a CUDA
+error.
 """
 from __future__ import annotations
 
@@ -17,19 +19,42 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_epi.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+UNITS = ["gemm_epi.cu", "spec_forward.cu", "spec_aux.cu"]
 
 
-def sources():
-    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
-             if f.endswith((".cu", ".cuh"))]
+def sources(csrc=CSRC):
+    files = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh"))]
     files.append(os.path.join(ROOT, "include", "gemm_epi.h"))
     return files
 
 
-def nvcc_command(out: str, extra=()):
-    return (["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",
-             "-shared", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"),
-             *extra, "-o", out, os.path.join(CSRC, "gemm_epi.cu")])
+def compile_command(src: str, obj: str, extra=()):
+    return ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), *extra,
+            "-c", "-o", obj, src]
+
+
+def link_command(objs, out: str):
+    return ["nvcc", *ARCH, "-shared", "-o", out, *objs]
+
+
+def compile_library(csrc: str, out: str, verbose: bool = False) -> str:
+    """Builds the library from the sources in `csrc` into `out`."""
+    obj_dir = out + ".objs"
+    os.makedirs(obj_dir, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if verbose else []
+    procs, objs = [], []
+    for unit in UNITS:
+        obj = os.path.join(obj_dir, unit.replace(".cu", ".o"))
+        objs.append(obj)
+        procs.append(subprocess.Popen(compile_command(os.path.join(csrc, unit), obj, extra)))
+    codes = [p.wait() for p in procs]
+    if any(codes):
+        raise RuntimeError("nvcc failed for %s" % [u for u, c in zip(UNITS, codes) if c])
+    tmp = out + ".tmp.%d" % os.getpid()
+    subprocess.run(link_command(objs, tmp), check=True)
+    os.replace(tmp, out)
+    return out
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -37,11 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             and os.path.getmtime(LIB) >= max(os.path.getmtime(f) for f in sources())):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = nvcc_command(tmp, ["-Xptxas", "-v"] if verbose else [])
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return compile_library(CSRC, LIB, verbose)
 
 
 if __name__ == "__main__":

@@ -41,6 +41,9 @@
 
 #include <stdint.h>
 
+#include <type_traits>
+#include <utility>
+
 #include "gemm_epi.h"
 #include "ptx.cuh"
 
@@ -148,6 +151,90 @@ struct KernelParams {
   EpiOpDev ops[GEMM_EPI_MAX_OPS];
 };
 
+// ------------------------------------------------------------------ programs
+//
+// The epilogue program reaches the kernel in one of two forms:
+//  - DynamicProgram: the op list is read from KernelParams and interpreted
+//    per 32-column chunk (any program create() accepts);
+//  - StaticProgram<ops...>: the op codes are template arguments, so every
+//    dispatch folds away and the kernel holds only the code of its own ops.
+//    Each entry is code | (pair group << 8).  Per-call values (alpha, bias,
+//    eps, ...) still come from KernelParams.
+// The library compiles static forms of the programs it is benchmarked on and
+// falls back to the interpreter for the rest; both run the same op bodies.
+
+struct DynamicProgram {
+  static constexpr bool is_static = false;
+};
+
+template <int... Ops>
+struct StaticProgram {
+  static constexpr bool is_static = true;
+  static constexpr int n = sizeof...(Ops);
+  static constexpr int code_of(int i) {
+    constexpr int c[] = {Ops..., 0};
+    return c[i] & 0xFF;
+  }
+  static constexpr int arg_of(int i) {
+    constexpr int c[] = {Ops..., 0};
+    return c[i] >> 8;
+  }
+  static constexpr int pair_at() {
+    for (int i = 0; i < n; ++i)
+      if (code_of(i) == GEMM_EPI_OP_PAIR_SWIGLU) return i;
+    return -1;
+  }
+  static constexpr int pair_g() {
+    return pair_at() < 0 ? 1 : (arg_of(pair_at()) == 0 ? 1 : arg_of(pair_at()));
+  }
+  static constexpr bool has(int code) {
+    for (int i = 0; i < n; ++i)
+      if (code_of(i) == code) return true;
+    return false;
+  }
+};
+
+template <int Begin, class F, int... Is>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, Is...>) {
+  (f(std::integral_constant<int, Begin + Is>{}), ...);
+}
+
+// f(integral_constant<int, i>) for i in [Begin, End), unrolled at compile time.
+template <int Begin, int End, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (End > Begin) static_for_impl<Begin>(f, std::make_integer_sequence<int, End - Begin>{});
+}
+
+template <class Prog>
+__host__ __device__ constexpr int prog_pair_at() {
+  if constexpr (Prog::is_static) return Prog::pair_at(); else return -1;
+}
+template <class Prog>
+__host__ __device__ constexpr int prog_pair_g() {
+  if constexpr (Prog::is_static) return Prog::pair_g(); else return 1;
+}
+template <class Prog>
+__host__ __device__ constexpr int prog_n() {
+  if constexpr (Prog::is_static) return Prog::n; else return 0;
+}
+
+// Flags a static program implies (F_ZERO_ACC stays a per-call flag).
+template <class Prog>
+__host__ __device__ constexpr uint32_t static_flags() {
+  if constexpr (!Prog::is_static) {
+    return 0u;
+  } else {
+    uint32_t f = 0;
+    if (Prog::has(GEMM_EPI_OP_ADD_RESIDUAL) || Prog::has(GEMM_EPI_OP_MUL_GELU_TANH_GRAD)) f |= F_AUX;
+    if (Prog::has(GEMM_EPI_OP_STORE_BF16)) f |= F_STORE;
+    if (Prog::has(GEMM_EPI_OP_STORE_E4M3)) f |= F_E8;
+    if (Prog::has(GEMM_EPI_OP_AMAX)) f |= F_AMAX;
+    if (Prog::has(GEMM_EPI_OP_ROW_RMS_RSQRT)) f |= F_ROW;
+    if (Prog::has(GEMM_EPI_OP_COL_SUM)) f |= F_COL;
+    return f;
+  }
+}
+
 // ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& mb, int& nb) {
@@ -195,7 +282,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Short bounded wait used while draining after an abort (no flag check).
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (!ptx::mbar_test(bar, parity)) {
@@ -251,11 +338,11 @@ __device__ __forceinline__ float bf16_round_f(float x) {
 
 // Element-wise ops that may run on accumulator columns (before the pair op)
 // or on output columns.  Columns of v[j]: col0 + j; `ncols` bounds the bias.
-template <int NV>
-__device__ __forceinline__ void apply_pointwise(const EpiOpDev& op, float (&v)[NV],
-                                                const KernelParams& p, int col0, int ncols,
-                                                float row_scale_m) {
-  switch (op.code) {
+// `code` is an int, or a std::integral_constant whose switch folds away.
+template <int NV, class CodeT>
+__device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], const KernelParams& p,
+                                                int col0, int ncols, float row_scale_m) {
+  switch (static_cast<int>(code)) {
     case GEMM_EPI_OP_SCALE_ALPHA:
 #pragma unroll
       for (int j = 0; j < NV; ++j) v[j] *= p.alpha;
@@ -336,7 +423,7 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 
 // ------------------------------------------------------------------ kernel
 
-template <int CG>
+template <int CG, class Prog>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tm_a,
                                const __grid_constant__ CUtensorMap tm_b,
@@ -536,11 +623,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------- epilogue
     const int ew = warp - 2;    // staging-buffer owner index 0..3
     const int quad = warp & 3;  // TMEM lane quadrant this warp may read
-    const int pair_at = p.pair_at;
+    constexpr bool kStatic = Prog::is_static;
+    const int pair_at = kStatic ? prog_pair_at<Prog>() : p.pair_at;
     const bool paired = pair_at >= 0;
     const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
     const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
-    const uint32_t flags = p.flags;
+    // A static program fixes every flag but the K == 0 one at compile time.
+    const uint32_t flags = kStatic ? (p.flags & F_ZERO_ACC) | static_flags<Prog>() : p.flags;
     const uint32_t epi0 = sbase + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
     const uint32_t e80 = sbase + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     uint8_t* epi0_ptr = smem + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
@@ -623,9 +712,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 64; ++j) a[j] = __uint_as_float(r[j]);
           }
-          for (int i = 0; i < pair_at; ++i)
-            apply_pointwise<64>(p.ops[i], a, p, nacc0 + c * 64, p.N, rs_m);
-          pair_swiglu(a, v, p.pair_g);
+          if constexpr (kStatic) {
+            static_for<0, (prog_pair_at<Prog>() < 0 ? 0 : prog_pair_at<Prog>())>([&](auto I) {
+              apply_pointwise<64>(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}, a, p,
+                                  nacc0 + c * 64, p.N, rs_m);
+            });
+            pair_swiglu_g<prog_pair_g<Prog>()>(a, v);
+          } else {
+            for (int i = 0; i < pair_at; ++i)
+              apply_pointwise<64>(p.ops[i].code, a, p, nacc0 + c * 64, p.N, rs_m);
+            pair_swiglu(a, v, p.pair_g);
+          }
         }
         if (c == chunks - 1) {
           // The accumulator buffer is free for the next tile's MMAs.
@@ -666,9 +763,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // ---- the op program on output columns
         const bool full_cols = col0 + 32 <= p.n_out;
-        for (int i = op_begin; i < p.n_ops; ++i) {
-          const EpiOpDev op = p.ops[i];
-          switch (op.code) {
+        // One body per op; `code` is an int (interpreted program) or an
+        // integral_constant (static program), for which the switch folds.
+        auto run_op = [&](auto code) {
+          switch (static_cast<int>(code)) {
             case GEMM_EPI_OP_ADD_RESIDUAL:
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] += x[j];
@@ -750,9 +848,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             default:
-              apply_pointwise<32>(op, v, p, col0, p.n_out, rs_m);
+              apply_pointwise<32>(code, v, p, col0, p.n_out, rs_m);
               break;
           }
+        };
+        if constexpr (kStatic) {
+          static_for<(prog_pair_at<Prog>() < 0 ? 0 : prog_pair_at<Prog>() + 1), prog_n<Prog>()>(
+              [&](auto I) { run_op(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}); });
+        } else {
+          for (int i = op_begin; i < p.n_ops; ++i) run_op(p.ops[i].code);
         }
 
         // ---- stores of this chunk, then the aux load AUX_AHEAD chunks ahead

@@ -23,7 +23,7 @@
 #include <vector>
 
 #include "gemm_epi.h"
-#include "fused_kernel.cuh"
+#include "programs.cuh"
 #include "unfused_kernel.cuh"
 
 namespace {
@@ -58,6 +58,10 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[128];
 
+// The interpreting kernels (any program); static ones come from the tables.
+const void* const kDynamic1 = reinterpret_cast<const void*>(&ge::fused_gemm_epilogue_kernel<1, ge::DynamicProgram>);
+const void* const kDynamic2 = reinterpret_cast<const void*>(&ge::fused_gemm_epilogue_kernel<2, ge::DynamicProgram>);
+
 // Scratch of gemm_epi_run_no_alloc: the status words and row counters that
 // gemm_epi_run keeps in the caller's workspace.  Every device that loads the
 // library holds this array until the process exits.  On the host its name is
@@ -79,11 +83,21 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
         (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if (d.cc_major == 10 && d.cc_minor == 3) {
-      e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel<1>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<1>::BYTES);
+      // Every compiled kernel needs the large dynamic shared memory opt-in.
+      e = cudaFuncSetAttribute(kDynamic1, cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<1>::BYTES);
       if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(ge::fused_gemm_epilogue_kernel<2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<2>::BYTES);
+        e = cudaFuncSetAttribute(kDynamic2, cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<2>::BYTES);
+      for (int t = 0; t < 2 && e == cudaSuccess; ++t) {
+        const ge::KernelSpec* tab = t == 0 ? ge::kSpecsForward : ge::kSpecsAux;
+        const int n = t == 0 ? ge::kNumSpecsForward : ge::kNumSpecsAux;
+        for (int i = 0; i < n && e == cudaSuccess; ++i) {
+          e = cudaFuncSetAttribute(tab[i].kernel_1sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   ge::Smem<1>::BYTES);
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tab[i].kernel_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     ge::Smem<2>::BYTES);
+        }
+      }
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
       // How many CTA pairs the GPU holds at once (a persistent grid larger
       // than that would leave pairs waiting for others to finish).
@@ -100,7 +114,7 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, ge::fused_gemm_epilogue_kernel<2>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&clusters, kDynamic2, &cfg);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
       d.pair_clusters = clusters;
     }
@@ -161,6 +175,7 @@ struct gemm_epi_plan {
   int rms_unrounded = 0;
   int64_t num_m_tiles = 0, num_n_tiles = 0;
   size_t ws_bytes = WS_HEADER;
+  const ge::KernelSpec* spec = nullptr;  // compiled form of the program, or NULL
 };
 
 namespace {
@@ -258,6 +273,23 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   // both main-loop shapes fit.
   const size_t row_blocks = static_cast<size_t>((d.M + 2 * ge::BLOCK_M - 1) / (2 * ge::BLOCK_M)) * 2;
   P.ws_bytes = WS_HEADER + ((row_blocks * 4 + 255) / 256) * 256;
+
+  // A compiled kernel whose op list (and pair group) is exactly this one.
+  P.spec = nullptr;
+  for (int t = 0; t < 2 && !P.spec; ++t) {
+    const ge::KernelSpec* tab = t == 0 ? ge::kSpecsForward : ge::kSpecsAux;
+    const int n = t == 0 ? ge::kNumSpecsForward : ge::kNumSpecsAux;
+    for (int i = 0; i < n && !P.spec; ++i) {
+      if (tab[i].n_ops != d.n_ops) continue;
+      bool same = true;
+      for (int j = 0; j < d.n_ops && same; ++j) {
+        const int c = d.ops[j].code;
+        const int enc = c | (c == GEMM_EPI_OP_PAIR_SWIGLU ? P.pair_g << 8 : 0);
+        same = enc == tab[i].ops[j];
+      }
+      if (same) P.spec = &tab[i];
+    }
+  }
   return GEMM_EPI_OK;
 }
 
@@ -265,7 +297,8 @@ struct Launch {
   CUtensorMap ta, tb, tc, tc8, taux;
   ge::KernelParams kp;
   int grid;
-  int cg;  // CTAs per tile: 1 (128 x 256) or 2 (a CTA pair, 256 x 256)
+  int cg;              // CTAs per tile: 1 (128 x 256) or 2 (a CTA pair, 256 x 256)
+  const void* kernel;  // static kernel of the plan's program, or the interpreting one
 };
 
 // 2-SM tiles unless the problem has a single 128-row block (then half of
@@ -284,6 +317,10 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   const gemm_epi_desc& d = P.d;
   std::memset(&L, 0, sizeof L);
   L.cg = choose_cta_group(P, a, dev);
+  if (P.spec && !(a.debug_flags & GEMM_EPI_DEBUG_FORCE_INTERPRETER))
+    L.kernel = L.cg == 2 ? P.spec->kernel_2sm : P.spec->kernel_1sm;
+  else
+    L.kernel = L.cg == 2 ? kDynamic2 : kDynamic1;
   const int tile_m = ge::BLOCK_M * L.cg;
   ge::KernelParams& k = L.kp;
   k.M = static_cast<int32_t>(d.M);
@@ -412,9 +449,9 @@ gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(ge::NUM_THREADS, 1, 1);
   cfg.stream = st;
-  cudaError_t e;
+  cudaLaunchAttribute attr;  // lives until the launch below
+  std::memset(&attr, 0, sizeof attr);
   if (L.cg == 2) {
-    cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
     attr.val.clusterDim.y = 1;
@@ -422,11 +459,13 @@ gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     cfg.dynamicSmemBytes = ge::Smem<2>::BYTES;
-    e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel<2>, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
   } else {
     cfg.dynamicSmemBytes = ge::Smem<1>::BYTES;
-    e = cudaLaunchKernelEx(&cfg, ge::fused_gemm_epilogue_kernel<1>, L.ta, L.tb, L.tc, L.tc8, L.taux, L.kp);
   }
+  void* params[] = {const_cast<CUtensorMap*>(&L.ta), const_cast<CUtensorMap*>(&L.tb),
+                    const_cast<CUtensorMap*>(&L.tc), const_cast<CUtensorMap*>(&L.tc8),
+                    const_cast<CUtensorMap*>(&L.taux), const_cast<ge::KernelParams*>(&L.kp)};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, L.kernel, params);
   return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the fused kernel");
 }
 

@@ -1,0 +1,62 @@
+// programs.cuh -- the epilogue programs compiled as static kernels.
+//
+// gemm_epi_create matches a plan's op list against these entries (codes and
+// pair group, in order); a match launches the static kernel, anything else
+// the interpreting one.  Per-call values (alpha, bias, eps, scales, ...) are
+// runtime arguments either way.
+#pragma once
+
+#include "fused_kernel.cuh"
+
+namespace ge {
+
+constexpr int PAIR_G1 = GEMM_EPI_OP_PAIR_SWIGLU | (1 << 8);
+
+// Bare GEMM: the store-only epilogue (also the first half of the unfused path).
+using ProgBare = StaticProgram<GEMM_EPI_OP_STORE_BF16>;
+// gelu_tanh(alpha * acc + bias), AMAX, bf16 store.
+using ProgBiasGelu = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_GELU_TANH,
+                                   GEMM_EPI_OP_AMAX, GEMM_EPI_OP_STORE_BF16>;
+// silu(gate) * up on even/odd columns, bf16 store.
+using ProgSwiGLU = StaticProgram<PAIR_G1, GEMM_EPI_OP_STORE_BF16>;
+// relu(alpha * acc + bias), AMAX, bf16 and e4m3 stores.
+using ProgFp8 = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_RELU,
+                              GEMM_EPI_OP_AMAX, GEMM_EPI_OP_STORE_BF16, GEMM_EPI_OP_STORE_E4M3>;
+// residual + acc, bf16 store, per-row rsqrt(mean square + eps).
+using ProgResidualRms = StaticProgram<GEMM_EPI_OP_ADD_RESIDUAL, GEMM_EPI_OP_STORE_BF16,
+                                      GEMM_EPI_OP_ROW_RMS_RSQRT>;
+// acc * gelu_tanh'(preact), bf16 store, column sums.
+using ProgGeluGradColSum = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16,
+                                         GEMM_EPI_OP_COL_SUM>;
+
+// One compiled program: its op list (code | pair group << 8) and its kernels
+// for the 1-SM and 2-SM main loops.
+struct KernelSpec {
+  const char* name;
+  int n_ops;
+  int ops[GEMM_EPI_MAX_OPS];
+  const void* kernel_1sm;
+  const void* kernel_2sm;
+};
+
+template <class Prog, int... Is>
+inline KernelSpec make_spec(const char* name, std::integer_sequence<int, Is...>) {
+  return KernelSpec{name,
+                    Prog::n,
+                    {(Prog::code_of(Is) | (Prog::arg_of(Is) << 8))...},
+                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<1, Prog>),
+                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<2, Prog>)};
+}
+
+template <class Prog>
+inline KernelSpec make_spec(const char* name) {
+  return make_spec<Prog>(name, std::make_integer_sequence<int, Prog::n>{});
+}
+
+// Tables defined by the translation units that instantiate the kernels.
+extern const KernelSpec kSpecsForward[];
+extern const int kNumSpecsForward;
+extern const KernelSpec kSpecsAux[];
+extern const int kNumSpecsAux;
+
+}  // namespace ge

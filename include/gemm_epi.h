@@ -173,6 +173,9 @@ typedef struct gemm_epi_args {
  * 2-SM loop runs when M > 128. */
 #define GEMM_EPI_DEBUG_FORCE_1SM 2u
 #define GEMM_EPI_DEBUG_FORCE_2SM 4u
+/* Test hook: run the op-interpreting kernel even when the program has a
+ * compiled (static) kernel, so both forms can be checked on one program. */
+#define GEMM_EPI_DEBUG_FORCE_INTERPRETER 8u
 
 typedef struct gemm_epi_plan *gemm_epi_handle;
 

@@ -45,8 +45,11 @@ SMALL_SHAPES = [
 
 
 # The two main-loop shapes: one CTA per 128 x 256 tile, or a CTA pair per
-# 256 x 256 tile (the default whenever M > 128).
-VARIANTS = {"1sm": native.GEMM_EPI_DEBUG_FORCE_1SM, "2sm": native.GEMM_EPI_DEBUG_FORCE_2SM}
+# 256 x 256 tile (the default whenever M > 128); and the op-interpreting
+# kernel in place of a program's compiled one.
+VARIANTS = {"1sm": native.GEMM_EPI_DEBUG_FORCE_1SM, "2sm": native.GEMM_EPI_DEBUG_FORCE_2SM,
+            "interp": native.GEMM_EPI_DEBUG_FORCE_INTERPRETER,
+            "interp1sm": native.GEMM_EPI_DEBUG_FORCE_INTERPRETER | native.GEMM_EPI_DEBUG_FORCE_1SM}
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
