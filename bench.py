@@ -21,6 +21,7 @@ import glob
 import hashlib
 import json
 import os
+import random
 import re
 import statistics
 import subprocess
@@ -336,19 +337,21 @@ def run_ours(args, world, rank, local):
         for f in (bare_step, unfused_step):
             for _ in range(3):
                 f()
-        n = max(3, min(args.steps // 4, 20))
+        n = max(3, min(args.steps // 4, 10))
         t = {"fused": [], "bare": [], "unfused": []}
-        for _ in range(7):
-            t["fused"].append(time_steps(step, n, stream) / n)
-            t["bare"].append(time_steps(bare_step, n, stream) / n)
-            t["unfused"].append(time_steps(unfused_step, n, stream) / n)
+        fns = [("fused", step), ("bare", bare_step), ("unfused", unfused_step)]
+        rng = random.Random(0)
+        for _ in range(15):
+            rng.shuffle(fns)  # no variant keeps a fixed place in the power-cap cycle
+            for name, fn in fns:
+                t[name].append(time_steps(fn, n, stream) / n)
         med = {k: statistics.median(v) for k, v in t.items()}
         extras = {
             "bare_gemm_ms": med["bare"] * 1e3, "bare_gemm_tflops": flops / med["bare"] / 1e12,
             "unfused_ms": med["unfused"] * 1e3, "unfused_tflops": flops / med["unfused"] / 1e12,
             "fused_ms_interleaved": med["fused"] * 1e3,
             "overhead_vs_bare": med["fused"] / med["bare"] - 1.0,
-            "comparison": "7 interleaved rounds of %d launches each, medians" % n,
+            "comparison": "15 rounds of %d launches each, order shuffled per round, medians" % n,
         }
         del bare_out, scratch
 

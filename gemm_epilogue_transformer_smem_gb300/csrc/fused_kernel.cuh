@@ -29,7 +29,8 @@
 //               tcgen05.ld (thread = row, register = column), runs the op
 //               program in registers, stages bf16 / e4m3 results in swizzled
 //               shared memory and writes them with TMA stores.  Residual and
-//               pre-activation tiles arrive by TMA two chunks ahead.
+//               pre-activation rows are read straight into registers one
+//               chunk ahead.
 // The accumulator is double-buffered, so a tile's epilogue overlaps the next
 // tile's main loop.  Tiles are walked persistently (grid = number of SMs) in
 // groups of `group_m` M-tiles so that neighbouring CTAs share A and B in L2.
@@ -56,8 +57,7 @@ constexpr int UMMA_K = 16;
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int CHUNK = 32;     // output columns per epilogue step
-constexpr int EPI_BUFS = 3;   // bf16 / aux staging buffers per epilogue warp
-constexpr int AUX_AHEAD = EPI_BUFS - 1;  // aux tiles loaded this many chunks ahead
+constexpr int EPI_BUFS = 3;   // bf16 output staging buffers per epilogue warp
 constexpr int E8_BUFS = 2;    // e4m3 staging buffers per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;
 
@@ -82,8 +82,7 @@ struct Smem {
   static constexpr uint32_t BAR_EMPTY = BAR_FULL + STAGES;
   static constexpr uint32_t BAR_TFULL = BAR_EMPTY + STAGES;
   static constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 2;
-  static constexpr uint32_t BAR_AUX = BAR_TEMPTY + 2;
-  static constexpr uint32_t BAR_DRAIN = BAR_AUX + NUM_EPI_WARPS * EPI_BUFS;
+  static constexpr uint32_t BAR_DRAIN = BAR_TEMPTY + 2;
   static constexpr uint32_t NUM_BARS = BAR_DRAIN + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;  // + room to align the base to 1 KB
@@ -109,7 +108,6 @@ enum : uint32_t {
   W_MMA_FULL = 2,
   W_MMA_TMEM_EMPTY = 3,
   W_EPI_TMEM_FULL = 4,
-  W_EPI_AUX = 5,
   W_DRAIN = 6,
 };
 
@@ -141,9 +139,11 @@ struct KernelParams {
   float* amax;
   float* row_out;
   float* col_out;
-  uint16_t* c;   // bf16 output (ragged-tail stores)
+  uint16_t* c;   // bf16 output (ragged-tail and direct stores)
   uint8_t* c8;   // e4m3 output (ragged-tail stores)
   int64_t ldc, ldc8;
+  const uint16_t* aux;  // residual or pre-activation (direct loads)
+  int64_t ld_aux;
   uint32_t* status;       // workspace: [0] error bits, [1] where, [2] block
   uint32_t* row_counter;  // workspace: one arrival counter per 128-row block
   uint64_t timeout_ns;
@@ -406,6 +406,29 @@ __device__ __forceinline__ void pair_swiglu(const float (&a)[64], float (&out)[3
   }
 }
 
+// This thread's 32 auxiliary bf16 values of row m, columns col0.. (zeros
+// outside the tensor), straight from global memory.
+__device__ __forceinline__ void load_aux_row(uint4 (&w)[4], const KernelParams& p, int m, bool row_ok,
+                                             int col0) {
+  if (row_ok && col0 + 32 <= p.n_out) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.aux + static_cast<int64_t>(m) * p.ld_aux + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = __ldg(src + q);
+  } else {
+    uint32_t h[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int n = col0 + 2 * j;
+      const uint16_t* rowp = p.aux + static_cast<int64_t>(m) * p.ld_aux;
+      const uint32_t lo = (row_ok && n < p.n_out) ? rowp[n] : 0u;
+      const uint32_t hi = (row_ok && n + 1 < p.n_out) ? rowp[n + 1] : 0u;
+      h[j] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+  }
+}
+
 // Lane l returns the sum over the warp's 32 lanes of x[l] (x is consumed).
 __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 #pragma unroll
@@ -429,13 +452,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                const __grid_constant__ CUtensorMap tm_b,
                                const __grid_constant__ CUtensorMap tm_c,
                                const __grid_constant__ CUtensorMap tm_c8,
-                               const __grid_constant__ CUtensorMap tm_aux,
                                const __grid_constant__ KernelParams p) {
   using L = Smem<CG>;
   constexpr int STAGES = L::STAGES;
   constexpr int TILE_M = BLOCK_M * CG;  // rows of one tile (the whole CTA group)
   constexpr uint32_t BAR_FULL = L::BAR_FULL, BAR_EMPTY = L::BAR_EMPTY, BAR_TFULL = L::BAR_TFULL,
-                     BAR_TEMPTY = L::BAR_TEMPTY, BAR_AUX = L::BAR_AUX, BAR_DRAIN = L::BAR_DRAIN;
+                     BAR_TEMPTY = L::BAR_TEMPTY, BAR_DRAIN = L::BAR_DRAIN;
   extern __shared__ uint8_t smem_raw[];
   // Same offset in both CTAs of a pair: the pair MMA addresses the peer's
   // operands and accumulator by this CTA's offsets.
@@ -462,7 +484,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(bar(BAR_TFULL + b), 1);
       ptx::mbar_init(bar(BAR_TEMPTY + b), NUM_EPI_WARPS * CG);  // every epilogue warp of the group
     }
-    for (uint32_t i = 0; i < NUM_EPI_WARPS * EPI_BUFS; ++i) ptx::mbar_init(bar(BAR_AUX + i), 1);
     ptx::mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -635,20 +656,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* epi0_ptr = smem + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
     uint8_t* e80_ptr = smem + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     const int op_begin = paired ? pair_at + 1 : 0;
-    const uint64_t aux_policy = ptx::policy_evict_first();
 
     uint32_t amax_bits = 0;
     uint32_t gchunk = 0;                 // this warp's running chunk number
-    uint32_t aux_issued = 0, aux_done = 0;  // chunk numbers of aux loads
     bool ok = true;
     int local = 0;
 
-    auto issue_aux = [&](uint32_t g, int col, int row0) {
-      const uint32_t i = g % EPI_BUFS;
-      const uint32_t b = bar(BAR_AUX + ew * EPI_BUFS + i);
-      ptx::mbar_arrive_expect_tx(b, EPI_BUF_BYTES);
-      ptx::tma_load_2d_hint(epi0 + i * EPI_BUF_BYTES, &tm_aux, b, col, row0, aux_policy);
-    };
 
     for (int t = group; ok && t < p.num_tiles; t += num_groups, ++local) {
       int mb, nb;
@@ -663,15 +676,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t buf = local & 1, use = local >> 1;
       const float rs_m = (p.row_scale != nullptr && row_ok) ? __ldg(p.row_scale + m) : 0.0f;
 
-      if (flags & F_AUX) {
-        if (lane == 0) {
-          ptx::bulk_wait_group_read<0>();
-          const int first = min(AUX_AHEAD, chunks);
-          for (int c = 0; c < first; ++c) issue_aux(gchunk + c, n0 + c * CHUNK, slab_row0);
-          aux_issued = gchunk + first;
-        }
-        __syncwarp();
-      }
+      // Residual / pre-activation rows are read straight into registers,
+      // one chunk ahead of their use (each thread reads its own row).
+      uint4 xa[4];
+      if (flags & F_AUX) load_aux_row(xa, p, m, row_ok, n0);
 
       // All lanes wait; the outcome is made warp-uniform so that no lane
       // leaves while the others enter a warp-synchronous step.
@@ -739,23 +747,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---- auxiliary tile (residual / pre-activation), this thread's row
         float x[32];
         if (flags & F_AUX) {
-          if (!__all_sync(0xffffffffu, wait_bar<CG>(bar(BAR_AUX + ew * EPI_BUFS + eb),
-                                                (g / EPI_BUFS) & 1u, abort_flag, p, W_EPI_AUX))) {
-            ok = false;
-            break;
-          }
-          aux_done = g + 1;
-          const uint8_t* rowp = epi0_ptr + eb * EPI_BUF_BYTES + lane * 64;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            const uint32_t ww[4] = {xa[q].x, xa[q].y, xa[q].z, xa[q].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               x[8 * q + 2 * h] = __uint_as_float(ww[h] << 16);
               x[8 * q + 2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
             }
           }
+          if (c + 1 < chunks) load_aux_row(xa, p, m, row_ok, n0 + (c + 1) * CHUNK);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = 0.0f;
@@ -806,8 +807,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             case GEMM_EPI_OP_STORE_E4M3: {
-              uint8_t* rowp = e80_ptr + (g % E8_BUFS) * E8_BUF_BYTES + lane * 32;
               const float s = p.fp8_scale;
+              uint8_t* rowp = e80_ptr + (g % E8_BUFS) * E8_BUF_BYTES + lane * 32;
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 uint32_t w[4];
@@ -859,26 +860,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = op_begin; i < p.n_ops; ++i) run_op(p.ops[i].code);
         }
 
-        // ---- stores of this chunk, then the aux load AUX_AHEAD chunks ahead
-        // into the buffer whose store (chunk g-1) has finished reading it.
-        if (flags & (F_STORE | F_E8 | F_AUX)) {
-          ptx::fence_proxy_async_smem();  // generic smem accesses before async-proxy ones
+        // ---- TMA stores of this chunk's staged outputs
+        if (flags & (F_STORE | F_E8)) {
+          ptx::fence_proxy_async_smem();  // generic smem writes before the async-proxy reads
           __syncwarp();
           if (lane == 0) {
-            if (flags & (F_STORE | F_E8)) {
-              if (slab_ok) {
-                if ((flags & F_STORE) && col0 < p.n_al)
-                  ptx::tma_store_2d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0);
-                if ((flags & F_E8) && col0 < p.n_al8)
-                  ptx::tma_store_2d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0);
-              }
-              ptx::bulk_commit_group();
-              ptx::bulk_wait_group_read<1>();
+            if (slab_ok) {
+              if ((flags & F_STORE) && col0 < p.n_al)
+                ptx::tma_store_2d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0);
+              if ((flags & F_E8) && col0 < p.n_al8)
+                ptx::tma_store_2d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0);
             }
-            if ((flags & F_AUX) && c + AUX_AHEAD < chunks) {
-              issue_aux(g + AUX_AHEAD, n0 + (c + AUX_AHEAD) * CHUNK, slab_row0);
-              aux_issued = g + AUX_AHEAD + 1;
-            }
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read<1>();  // the buffer of chunk g-1 is free again
           }
         }
         __syncwarp();
@@ -910,12 +904,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     // ---- teardown of the epilogue warp
-    if (lane == 0) {
-      ptx::bulk_wait_group<0>();
-      // Aux loads still in flight after an abort land before the CTA exits.
-      for (uint32_t g = aux_done; g < aux_issued; ++g)
-        drain_wait(bar(BAR_AUX + ew * EPI_BUFS + g % EPI_BUFS), (g / EPI_BUFS) & 1u, DRAIN_LIMIT_NS);
-    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
     if (flags & F_AMAX) {
 #pragma unroll
       for (int s = 16; s >= 1; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, s));

@@ -294,7 +294,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 }
 
 struct Launch {
-  CUtensorMap ta, tb, tc, tc8, taux;
+  CUtensorMap ta, tb, tc, tc8;
   ge::KernelParams kp;
   int grid;
   int cg;              // CTAs per tile: 1 (128 x 256) or 2 (a CTA pair, 256 x 256)
@@ -356,6 +356,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.c8 = static_cast<uint8_t*>(a.C8);
   k.ldc = d.ldc;
   k.ldc8 = d.ldc8;
+  k.aux = static_cast<const uint16_t*>(P.uses_residual ? a.residual : a.preact);
+  k.ld_aux = d.ld_aux;
   k.status = static_cast<uint32_t*>(a.workspace);
   k.row_counter = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + WS_HEADER);
   k.timeout_ns = static_cast<uint64_t>(a.timeout_ms ? a.timeout_ms : DEFAULT_TIMEOUT_MS) * 1000000ull;
@@ -391,12 +393,6 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   if ((P.flags & ge::F_E8) && k.n_al8 > 0) {
     s = make_map(&L.tc8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.C8, k.n_al8, d.M, d.ldc8, ge::CHUNK, 32,
                  CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C8");
-    if (s) return s;
-  }
-  if (P.flags & ge::F_AUX) {
-    const void* aux = P.uses_residual ? a.residual : a.preact;
-    s = make_map(&L.taux, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, aux, P.n_out, d.M, d.ld_aux * 2, ge::CHUNK, 32,
-                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, "aux");
     if (s) return s;
   }
   return GEMM_EPI_OK;
@@ -464,7 +460,7 @@ gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
   }
   void* params[] = {const_cast<CUtensorMap*>(&L.ta), const_cast<CUtensorMap*>(&L.tb),
                     const_cast<CUtensorMap*>(&L.tc), const_cast<CUtensorMap*>(&L.tc8),
-                    const_cast<CUtensorMap*>(&L.taux), const_cast<ge::KernelParams*>(&L.kp)};
+                    const_cast<ge::KernelParams*>(&L.kp)};
   const cudaError_t e = cudaLaunchKernelExC(&cfg, L.kernel, params);
   return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the fused kernel");
 }

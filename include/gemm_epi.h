@@ -58,10 +58,8 @@
  *    multiple of 8 (operand rows are read in whole 16-byte groups, so a
  *    ragged K tail would read the row padding); anything else is
  *    GEMM_EPI_ERR_MISALIGNED.  N and M need no alignment: outputs are written
- *    exactly within [0, M) x [0, N_out).  Inputs whose logical row width is
- *    not a multiple of 16 bytes (B with N % 8 != 0, residual / preact with
- *    N_out % 8 != 0) may have the rest of their last 16-byte group read; those
- *    values never reach an output.
+ *    exactly within [0, M) x [0, N_out).  B with N % 8 != 0 may have the rest
+ *    of its last 16-byte group read; those values never reach an output.
  *
  * Errors
  *  - create / run return synchronous validation errors and never launch
