@@ -5,7 +5,7 @@ method happens here; every step runs in the CUDA library.
 Programs are written as op names (one optional numeric argument after a
 colon):
 
-  alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g],
+  alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
   gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
   row_rms_unrounded[:eps], col_sum
 """
@@ -28,6 +28,7 @@ PROGRAM_OPS = {
     "relu": N.GEMM_EPI_OP_ACT_RELU,
     "silu": N.GEMM_EPI_OP_ACT_SILU,
     "pair_swiglu": N.GEMM_EPI_OP_PAIR_SWIGLU,
+    "pair_mul": N.GEMM_EPI_OP_PAIR_MUL,
     "gelu_tanh_grad": N.GEMM_EPI_OP_MUL_GELU_TANH_GRAD,
     "amax": N.GEMM_EPI_OP_AMAX,
     "store_bf16": N.GEMM_EPI_OP_STORE_BF16,
@@ -46,7 +47,7 @@ def encode_program(program: Sequence[str]):
             raise ValueError("unknown epilogue op %r" % name)
         code = PROGRAM_OPS[name]
         i0, f0 = 0, 0.0
-        if name == "pair_swiglu":
+        if name in ("pair_swiglu", "pair_mul"):
             i0 = int(arg) if arg else 1
         elif name.startswith("row_rms"):
             f0 = float(arg) if arg else 1e-6
@@ -65,22 +66,24 @@ class Plan:
 
     def __init__(self, M: int, N_: int, K: int, program: Sequence[str], b_layout: str = "kn",
                  lda: Optional[int] = None, ldb: Optional[int] = None, ldc: Optional[int] = None,
-                 ldc8: Optional[int] = None, ld_aux: Optional[int] = None):
+                 ldc8: Optional[int] = None, ld_aux: Optional[int] = None, dual: bool = False):
         self.lib = N.load()
         self.program = list(program)
         self.M, self.N, self.K = M, N_, K
         self.b_layout = b_layout
-        pair = any(op.startswith("pair_swiglu") for op in program)
+        pair = any(op.startswith("pair_") for op in program)
         n_out = N_ // 2 if pair else N_
         self._ops = encode_program(program)
         d = N.gemm_epi_desc()
         d.M, d.N, d.K = M, N_, K
         d.lda = K if lda is None else lda
-        d.ldb = (N_ if b_layout == "kn" else K) if ldb is None else ldb
+        b_cols = N_ // 2 if dual else N_
+        d.ldb = (b_cols if b_layout == "kn" else K) if ldb is None else ldb
         d.ldc = n_out if ldc is None else ldc
         d.ldc8 = n_out if ldc8 is None else ldc8
         d.ld_aux = n_out if ld_aux is None else ld_aux
-        d.b_layout = N.GEMM_EPI_B_KN if b_layout == "kn" else N.GEMM_EPI_B_NK
+        d.b_layout = (N.GEMM_EPI_B_KN if b_layout == "kn" else N.GEMM_EPI_B_NK) | (N.GEMM_EPI_B_DUAL if dual else 0)
+        self.dual = dual
         d.n_ops = len(program)
         d.ops = ctypes.cast(self._ops, ctypes.POINTER(N.gemm_epi_op))
         self.desc = d
@@ -98,9 +101,9 @@ class Plan:
 
     def args(self, A, B, *, alpha=1.0, fp8_scale=1.0, bias=None, row_scale=None, residual=None,
              preact=None, C=None, C8=None, amax=None, row_out=None, col_out=None, workspace=None,
-             timeout_ms=0, debug_flags=0) -> N.gemm_epi_args:
+             timeout_ms=0, debug_flags=0, B2=None) -> N.gemm_epi_args:
         a = N.gemm_epi_args()
-        a.A, a.B = _ptr(A), _ptr(B)
+        a.A, a.B, a.B2 = _ptr(A), _ptr(B), _ptr(B2)
         a.alpha, a.fp8_scale = float(alpha), float(fp8_scale)
         a.bias, a.row_scale = _ptr(bias), _ptr(row_scale)
         a.residual, a.preact = _ptr(residual), _ptr(preact)

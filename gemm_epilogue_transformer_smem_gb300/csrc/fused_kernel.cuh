@@ -127,11 +127,13 @@ struct KernelParams {
   int32_t num_m_tiles, num_n_tiles, num_tiles, num_k_blocks;
   int32_t group_m;
   int32_t b_kn;  // 1: B stored K x N (MN-major operand)
+  int32_t dual;  // 1: accumulator columns alternate between B and B2 in 128-column blocks
   uint32_t idesc;
   uint32_t flags;
   int32_t n_ops;
   int32_t pair_at;  // index of PAIR_SWIGLU in ops, or -1
   int32_t pair_g;
+  int32_t pair_silu;  // 1: SwiGLU pair, 0: plain product
   float alpha, fp8_scale, rms_eps;
   int32_t rms_unrounded;
   const float* bias;
@@ -181,7 +183,7 @@ struct StaticProgram {
   }
   static constexpr int pair_at() {
     for (int i = 0; i < n; ++i)
-      if (code_of(i) == GEMM_EPI_OP_PAIR_SWIGLU) return i;
+      if (code_of(i) == GEMM_EPI_OP_PAIR_SWIGLU || code_of(i) == GEMM_EPI_OP_PAIR_MUL) return i;
     return -1;
   }
   static constexpr int pair_g() {
@@ -212,6 +214,14 @@ __host__ __device__ constexpr int prog_pair_at() {
 template <class Prog>
 __host__ __device__ constexpr int prog_pair_g() {
   if constexpr (Prog::is_static) return Prog::pair_g(); else return 1;
+}
+template <class Prog>
+__host__ __device__ constexpr bool prog_pair_silu() {
+  if constexpr (Prog::is_static) {
+    return Prog::pair_at() >= 0 && Prog::code_of(Prog::pair_at()) == GEMM_EPI_OP_PAIR_SWIGLU;
+  } else {
+    return true;
+  }
 }
 template <class Prog>
 __host__ __device__ constexpr int prog_n() {
@@ -385,25 +395,35 @@ __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], cons
   }
 }
 
-// out[j] = silu(a[gate(j)]) * a[up(j)] with gate(j) = (j/G)*2G + j%G, up = gate + G.
-template <int G>
-__device__ __forceinline__ void pair_swiglu_g(const float (&a)[64], float (&out)[32]) {
+// out[j] = silu(a[gate(j)]) * a[up(j)] (SwiGLU) or a[gate(j)] * a[up(j)]
+// (the RMSNorm-MLP's plain product), gate(j) = (j/G)*2G + j%G, up = gate + G.
+template <int G, bool SILU>
+__device__ __forceinline__ void pair_combine_g(const float (&a)[64], float (&out)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int gate = (j / G) * 2 * G + (j % G);
-    out[j] = silu_f(a[gate]) * a[gate + G];
+    out[j] = (SILU ? silu_f(a[gate]) : a[gate]) * a[gate + G];
   }
 }
 
-__device__ __forceinline__ void pair_swiglu(const float (&a)[64], float (&out)[32], int g) {
+template <bool SILU>
+__device__ __forceinline__ void pair_combine_s(const float (&a)[64], float (&out)[32], int g) {
   switch (g) {
-    case 2: pair_swiglu_g<2>(a, out); break;
-    case 4: pair_swiglu_g<4>(a, out); break;
-    case 8: pair_swiglu_g<8>(a, out); break;
-    case 16: pair_swiglu_g<16>(a, out); break;
-    case 32: pair_swiglu_g<32>(a, out); break;
-    default: pair_swiglu_g<1>(a, out); break;
+    case 2: pair_combine_g<2, SILU>(a, out); break;
+    case 4: pair_combine_g<4, SILU>(a, out); break;
+    case 8: pair_combine_g<8, SILU>(a, out); break;
+    case 16: pair_combine_g<16, SILU>(a, out); break;
+    case 32:
+    case 128: pair_combine_g<32, SILU>(a, out); break;  // 128: the halves were loaded as 32 | 32
+    default: pair_combine_g<1, SILU>(a, out); break;
   }
+}
+
+__device__ __forceinline__ void pair_combine(const float (&a)[64], float (&out)[32], int g, bool silu) {
+  if (silu)
+    pair_combine_s<true>(a, out, g);
+  else
+    pair_combine_s<false>(a, out, g);
 }
 
 // This thread's 32 auxiliary bf16 values of row m, columns col0.. (zeros
@@ -450,6 +470,7 @@ template <int CG, class Prog>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tm_a,
                                const __grid_constant__ CUtensorMap tm_b,
+                               const __grid_constant__ CUtensorMap tm_b2,
                                const __grid_constant__ CUtensorMap tm_c,
                                const __grid_constant__ CUtensorMap tm_c8,
                                const __grid_constant__ KernelParams p) {
@@ -519,7 +540,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int a_row = mb * TILE_M + rank * BLOCK_M;
-        const int b_col = nb * BLOCK_N + rank * L::B_COLS;
+        // B columns of this tile.  With two weight operands, tile nb covers
+        // columns [nb*128, nb*128+128) of B (accumulator columns 0..127) and
+        // the same columns of B2 (accumulator columns 128..255).
+        const int b_col = p.dual ? nb * (BLOCK_N / 2) : nb * BLOCK_N + rank * L::B_COLS;
+        const CUtensorMap* tmb_own = (p.dual && rank == 1) ? &tm_b2 : &tm_b;  // 2-SM: one operand per CTA
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!wait_bar<CG>(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
             ok = false;
@@ -536,8 +561,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, a_row);
               if (p.b_kn) {
 #pragma unroll
-                for (int j = 0; j < L::B_COLS / 64; ++j)
-                  ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, &tm_b, fb, b_col + j * 64, kb * BLOCK_K);
+                for (int j = 0; j < L::B_COLS / 64; ++j) {
+                  // with B2, boxes 0-1 come from B and 2-3 from B2
+                  const bool second = p.dual && j >= 2;
+                  const int col = p.dual ? b_col + (j & 1) * 64 : b_col + j * 64;
+                  ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, second ? &tm_b2 : &tm_b, fb, col, kb * BLOCK_K);
+                }
+              } else if (p.dual) {
+                // two 128-row K-major boxes, one per operand, stacked in the stage
+                ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, b_col);
+                ptx::tma_load_2d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * BLOCK_K, b_col);
               } else {
                 ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, b_col);
               }
@@ -550,9 +583,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j)
-                  ptx::tma_load_2d_cg2(sb + j * B_MN_BOX_BYTES, &tm_b, fb0, b_col + j * 64, kb * BLOCK_K);
+                  ptx::tma_load_2d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K);
               } else {
-                ptx::tma_load_2d_cg2(sb, &tm_b, fb0, kb * BLOCK_K, b_col);
+                ptx::tma_load_2d_cg2(sb, tmb_own, fb0, kb * BLOCK_K, b_col);
               }
             }
             issued |= 1u << stage;
@@ -647,6 +680,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr bool kStatic = Prog::is_static;
     const int pair_at = kStatic ? prog_pair_at<Prog>() : p.pair_at;
     const bool paired = pair_at >= 0;
+    const bool pair_g128 = paired && (kStatic ? prog_pair_g<Prog>() == 128 : p.pair_g == 128);
     const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
     const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
     // A static program fixes every flag but the K == 0 one at compile time.
@@ -716,7 +750,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < 64; ++j) a[j] = 0.0f;
           } else {
             uint32_t r[64];
-            ptx::tmem_ld64_sync(t_row + c * 64, r);
+            // Groups up to 32 pair within 64 adjacent columns; group 128
+            // pairs column j of the tile's first half with j of its second.
+            if (pair_g128)
+              ptx::tmem_ld64_sync(t_row + c * 32, t_row + BLOCK_N / 2 + c * 32, r);
+            else
+              ptx::tmem_ld64_sync(t_row + c * 64, t_row + c * 64 + 32, r);
 #pragma unroll
             for (int j = 0; j < 64; ++j) a[j] = __uint_as_float(r[j]);
           }
@@ -725,11 +764,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               apply_pointwise<64>(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}, a, p,
                                   nacc0 + c * 64, p.N, rs_m);
             });
-            pair_swiglu_g<prog_pair_g<Prog>()>(a, v);
+            pair_combine_g<(prog_pair_g<Prog>() == 128 ? 32 : prog_pair_g<Prog>()), prog_pair_silu<Prog>()>(a, v);
           } else {
             for (int i = 0; i < pair_at; ++i)
               apply_pointwise<64>(p.ops[i].code, a, p, nacc0 + c * 64, p.N, rs_m);
-            pair_swiglu(a, v, p.pair_g);
+            pair_combine(a, v, p.pair_g, p.pair_silu != 0);
           }
         }
         if (c == chunks - 1) {

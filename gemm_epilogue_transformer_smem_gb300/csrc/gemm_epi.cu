@@ -168,7 +168,8 @@ struct gemm_epi_plan {
   gemm_epi_desc d;
   std::vector<gemm_epi_op> ops;
   int64_t n_out = 0;
-  int pair_at = -1, pair_g = 1;
+  int pair_at = -1, pair_g = 1, pair_silu = 1;
+  bool dual = false;  // GEMM_EPI_B_DUAL: B columns alternate with B2 in 128-column blocks
   uint32_t flags = 0;
   bool uses_bias = false, uses_row_scale = false, uses_residual = false, uses_preact = false;
   float rms_eps = 0.0f;
@@ -185,8 +186,13 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   const int64_t LIM = 0x7FFFFFFF;
   if (d.M < 0 || d.N < 0 || d.K < 0 || d.M > LIM || d.N > LIM || d.K > LIM)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "M, N, K must be in [0, 2^31)");
-  if (d.b_layout != GEMM_EPI_B_KN && d.b_layout != GEMM_EPI_B_NK)
+  const int b_base = d.b_layout & ~GEMM_EPI_B_DUAL;
+  P.dual = (d.b_layout & GEMM_EPI_B_DUAL) != 0;
+  if (b_base != GEMM_EPI_B_KN && b_base != GEMM_EPI_B_NK)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "unknown b_layout %d", d.b_layout);
+  if (P.dual && d.N % 256 != 0)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "GEMM_EPI_B_DUAL needs N %% 256 == 0 (N=%lld)",
+                static_cast<long long>(d.N));
   if (d.n_ops < 0 || d.n_ops > GEMM_EPI_MAX_OPS)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "n_ops must be in [0, %d]", GEMM_EPI_MAX_OPS);
   if (d.n_ops > 0 && !d.ops) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ops is NULL");
@@ -194,26 +200,35 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   int seen[16] = {0};
   for (int i = 0; i < d.n_ops; ++i) {
     const gemm_epi_op& op = d.ops[i];
-    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_COL_SUM)
+    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_PAIR_MUL)
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: unknown code %d", i, op.code);
     if (is_output_op(op.code) && seen[op.code])
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: output op %d appears twice", i, op.code);
     seen[op.code]++;
     switch (op.code) {
-      case GEMM_EPI_OP_PAIR_SWIGLU: {
-        if (P.pair_at >= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU appears twice");
+      case GEMM_EPI_OP_PAIR_SWIGLU:
+      case GEMM_EPI_OP_PAIR_MUL: {
+        if (P.pair_at >= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "a program has at most one pair op");
         int g = op.i0 == 0 ? 1 : op.i0;
-        if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32)
-          return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU group %d not in {1,2,4,8,16,32}", op.i0);
+        if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32 && g != 128)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "pair group %d not in {1,2,4,8,16,32,128}", op.i0);
+        if (P.dual && g != 128)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "with GEMM_EPI_B_DUAL the pair group must be 128");
         if (d.N % (2 * g) != 0)
           return fail(GEMM_EPI_ERR_INVALID_VALUE, "PAIR_SWIGLU group %d needs N %% %d == 0 (N=%lld)", g,
                       2 * g, static_cast<long long>(d.N));
-        for (int j = 0; j < i; ++j)
+        for (int j = 0; j < i; ++j) {
           if (!is_pre_pair_op(d.ops[j].code))
-            return fail(GEMM_EPI_ERR_UNSUPPORTED, "op %d (code %d) before PAIR_SWIGLU is not supported", j,
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "op %d (code %d) before a pair op is not supported", j,
                         d.ops[j].code);
+          // Group 128 pairs columns 128 apart within a tile, so a column bias
+          // before it would have to follow that layout; not offered.
+          if (g == 128 && d.ops[j].code == GEMM_EPI_OP_ADD_BIAS_COL)
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "ADD_BIAS_COL before a pair op of group 128");
+        }
         P.pair_at = i;
         P.pair_g = g;
+        P.pair_silu = op.code == GEMM_EPI_OP_PAIR_SWIGLU ? 1 : 0;
         break;
       }
       case GEMM_EPI_OP_ROW_RMS_RSQRT:
@@ -245,12 +260,13 @@ gemm_epi_status validate(gemm_epi_plan& P) {
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT over zero columns is undefined");
 
   // Strides: bounds first, then the 16-byte TMA rule.
-  const bool kn = d.b_layout == GEMM_EPI_B_KN;
+  const bool kn = b_base == GEMM_EPI_B_KN;
+  const int64_t b_cols = P.dual ? d.N / 2 : d.N;  // columns of each B operand
   if (d.K % 8)  // the K tail of a TMA box is clipped in 16-byte groups
     return fail(GEMM_EPI_ERR_MISALIGNED, "K must be a multiple of 8 (got %lld)", static_cast<long long>(d.K));
   if (d.K > 0) {  // A and B are not read when K == 0
     if (d.lda < d.K) return fail(GEMM_EPI_ERR_INVALID_VALUE, "lda < K");
-    if (d.ldb < (kn ? d.N : d.K) || d.ldb <= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldb too small");
+    if (d.ldb < (kn ? b_cols : d.K) || d.ldb <= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldb too small");
     if (d.lda % 8 || d.ldb % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "lda and ldb must be multiples of 8");
   }
   if ((P.flags & ge::F_STORE) && (d.ldc < P.n_out || d.ldc <= 0))
@@ -284,7 +300,8 @@ gemm_epi_status validate(gemm_epi_plan& P) {
       bool same = true;
       for (int j = 0; j < d.n_ops && same; ++j) {
         const int c = d.ops[j].code;
-        const int enc = c | (c == GEMM_EPI_OP_PAIR_SWIGLU ? P.pair_g << 8 : 0);
+        const bool pair = c == GEMM_EPI_OP_PAIR_SWIGLU || c == GEMM_EPI_OP_PAIR_MUL;
+        const int enc = c | (pair ? P.pair_g << 8 : 0);
         same = enc == tab[i].ops[j];
       }
       if (same) P.spec = &tab[i];
@@ -294,7 +311,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 }
 
 struct Launch {
-  CUtensorMap ta, tb, tc, tc8;
+  CUtensorMap ta, tb, tb2, tc, tc8;
   ge::KernelParams kp;
   int grid;
   int cg;              // CTAs per tile: 1 (128 x 256) or 2 (a CTA pair, 256 x 256)
@@ -334,7 +351,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.num_tiles = k.num_m_tiles * k.num_n_tiles;
   k.num_k_blocks = static_cast<int32_t>((d.K + ge::BLOCK_K - 1) / ge::BLOCK_K);
   k.group_m = DEFAULT_GROUP_M;
-  k.b_kn = d.b_layout == GEMM_EPI_B_KN ? 1 : 0;
+  k.b_kn = (d.b_layout & ~GEMM_EPI_B_DUAL) == GEMM_EPI_B_KN ? 1 : 0;
+  k.dual = P.dual ? 1 : 0;
   // Instruction descriptor: D fp32, A and B bf16, A K-major, B K- or
   // MN-major, N = 256, M = 128 per CTA of the group.
   k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (k.b_kn ? (1u << 16) : 0u) |
@@ -343,6 +361,7 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.n_ops = static_cast<int32_t>(P.ops.size());
   k.pair_at = P.pair_at;
   k.pair_g = P.pair_g;
+  k.pair_silu = P.pair_silu;
   k.alpha = a.alpha;
   k.fp8_scale = a.fp8_scale;
   k.rms_eps = P.rms_eps;
@@ -377,13 +396,21 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
     s = make_map(&L.ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, d.K, d.M, d.lda * 2, ge::BLOCK_K, ge::BLOCK_M,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
     if (s) return s;
-    if (k.b_kn)
-      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.N, d.K, d.ldb * 2, 64, ge::BLOCK_K,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
-    else
-      s = make_map(&L.tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, d.K, d.N, d.ldb * 2, ge::BLOCK_K,
-                   ge::BLOCK_N / L.cg, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
-    if (s) return s;
+    // Each B operand: N (or N/2 with B2) columns; K-major boxes hold the
+    // rows one CTA stages from one operand.
+    const int64_t b_cols = P.dual ? d.N / 2 : d.N;
+    const uint32_t nk_rows = (P.dual || L.cg == 2) ? ge::BLOCK_N / 2 : ge::BLOCK_N;
+    for (int which = 0; which < (P.dual ? 2 : 1); ++which) {
+      CUtensorMap* map = which == 0 ? &L.tb : &L.tb2;
+      const void* base = which == 0 ? a.B : a.B2;
+      if (k.b_kn)
+        s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, b_cols, d.K, d.ldb * 2, 64, ge::BLOCK_K,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B");
+      else
+        s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d.K, b_cols, d.ldb * 2, ge::BLOCK_K, nk_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B");
+      if (s) return s;
+    }
   }
   if ((P.flags & ge::F_STORE) && k.n_al > 0) {
     s = make_map(&L.tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, k.n_al, d.M, d.ldc * 2, ge::CHUNK, 32,
@@ -409,6 +436,7 @@ gemm_epi_status check_args(const gemm_epi_plan& P, const gemm_epi_args& a) {
   gemm_epi_status s;
   if (work && d.K > 0) {
     if ((s = need(a.A, "A")) || (s = need(a.B, "B"))) return s;
+    if (P.dual && (s = need(a.B2, "B2"))) return s;
   }
   if (work) {
     if ((P.flags & ge::F_STORE) && (s = need(a.C, "C"))) return s;
@@ -459,6 +487,7 @@ gemm_epi_status launch_fused(const Launch& L, cudaStream_t st) {
     cfg.dynamicSmemBytes = ge::Smem<1>::BYTES;
   }
   void* params[] = {const_cast<CUtensorMap*>(&L.ta), const_cast<CUtensorMap*>(&L.tb),
+                    const_cast<CUtensorMap*>(&L.tb2),
                     const_cast<CUtensorMap*>(&L.tc), const_cast<CUtensorMap*>(&L.tc8),
                     const_cast<ge::KernelParams*>(&L.kp)};
   const cudaError_t e = cudaLaunchKernelExC(&cfg, L.kernel, params);
@@ -554,6 +583,7 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   u.n_out = static_cast<int32_t>(h->n_out);
   u.pair_at = h->pair_at;
   u.pair_g = h->pair_g;
+  u.pair_silu = h->pair_silu;
   u.n_ops = static_cast<int32_t>(h->ops.size());
   u.flags = h->flags;
   u.alpha = args->alpha;

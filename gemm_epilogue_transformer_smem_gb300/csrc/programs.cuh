@@ -11,6 +11,9 @@
 namespace ge {
 
 constexpr int PAIR_G1 = GEMM_EPI_OP_PAIR_SWIGLU | (1 << 8);
+constexpr int PAIR_MUL_G1 = GEMM_EPI_OP_PAIR_MUL | (1 << 8);
+constexpr int PAIR_G128 = GEMM_EPI_OP_PAIR_SWIGLU | (128 << 8);
+constexpr int PAIR_MUL_G128 = GEMM_EPI_OP_PAIR_MUL | (128 << 8);
 
 // Bare GEMM: the store-only epilogue (also the first half of the unfused path).
 using ProgBare = StaticProgram<GEMM_EPI_OP_STORE_BF16>;
@@ -19,6 +22,14 @@ using ProgBiasGelu = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS
                                    GEMM_EPI_OP_AMAX, GEMM_EPI_OP_STORE_BF16>;
 // silu(gate) * up on even/odd columns, bf16 store.
 using ProgSwiGLU = StaticProgram<PAIR_G1, GEMM_EPI_OP_STORE_BF16>;
+// RMSNorm-consuming up-projections: rows scaled by the previous layer's S,
+// then silu(gate) * up or the plain gate * up, bf16 store.
+using ProgRmsSwiGLU = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, PAIR_G1, GEMM_EPI_OP_STORE_BF16>;
+using ProgRmsGlu = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, PAIR_MUL_G1, GEMM_EPI_OP_STORE_BF16>;
+// The same with separate gate / up weights (GEMM_EPI_B_DUAL, pair group 128).
+using ProgSwiGLU2W = StaticProgram<PAIR_G128, GEMM_EPI_OP_STORE_BF16>;
+using ProgRmsSwiGLU2W = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, PAIR_G128, GEMM_EPI_OP_STORE_BF16>;
+using ProgRmsGlu2W = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, PAIR_MUL_G128, GEMM_EPI_OP_STORE_BF16>;
 // relu(alpha * acc + bias), AMAX, bf16 and e4m3 stores.
 using ProgFp8 = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_RELU,
                               GEMM_EPI_OP_AMAX, GEMM_EPI_OP_STORE_BF16, GEMM_EPI_OP_STORE_E4M3>;

@@ -283,8 +283,9 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
-// Two 32-column loads (columns c and c + 32 of the same lanes) and one wait.
-__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
+// Two 32-column loads of the same lanes (at column addresses taddr0 and
+// taddr1) and one wait.
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr0, uint32_t taddr1, uint32_t (&r)[64]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -304,7 +305,7 @@ __device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]
         "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
         "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr), "r"(taddr + 32u)
+      : "r"(taddr0), "r"(taddr1)
       : "memory");
 }
 

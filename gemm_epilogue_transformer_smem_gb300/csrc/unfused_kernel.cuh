@@ -22,6 +22,7 @@ constexpr int UF_THREADS = 256;
 struct UnfusedParams {
   int32_t M, N, n_out;
   int32_t pair_at, pair_g, n_ops;
+  int32_t pair_silu;  // 1: SwiGLU pair, 0: plain product
   uint32_t flags;
   float alpha, fp8_scale, rms_eps;
   int32_t rms_unrounded;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(UF_THREADS)
           if (q == gate) ga = a[q];
           if (q == gate + g) ua = a[q];
         }
-        v[j] = silu_f(ga) * ua;
+        v[j] = (p.pair_silu ? silu_f(ga) : ga) * ua;
       }
     }
     float x[8];

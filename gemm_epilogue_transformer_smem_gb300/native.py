@@ -29,6 +29,7 @@ STATUS_NAMES = {
 # gemm_epi_b_layout
 GEMM_EPI_B_KN = 0
 GEMM_EPI_B_NK = 1
+GEMM_EPI_B_DUAL = 16
 
 # gemm_epi_op_code
 GEMM_EPI_OP_SCALE_ALPHA = 1
@@ -45,6 +46,7 @@ GEMM_EPI_OP_STORE_BF16 = 11
 GEMM_EPI_OP_STORE_E4M3 = 12
 GEMM_EPI_OP_ROW_RMS_RSQRT = 13
 GEMM_EPI_OP_COL_SUM = 14
+GEMM_EPI_OP_PAIR_MUL = 15
 
 GEMM_EPI_MAX_OPS = 16
 GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1
@@ -78,6 +80,7 @@ class gemm_epi_args(ctypes.Structure):
         ("amax", ctypes.c_void_p), ("row_out", ctypes.c_void_p), ("col_out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("timeout_ms", ctypes.c_uint32), ("debug_flags", ctypes.c_uint32),
+        ("B2", ctypes.c_void_p),
     ]
 
 

@@ -16,11 +16,14 @@ them; "N(0, s)" has standard deviation s):
   downproj  out = residual + A@B, per-row rsqrt(mean(out^2) + 1e-6).
             A 16384x14336 N(0,1)/sqrt(14336); B 14336x4096 N(0, 0.02);
             residual 16384x4096 N(0,1).
+  swiglu2w  the same up-projection with separate gate and up weights:
+            out = silu(A @ W_gate) * (A @ W_up), W_gate and W_up 4096x14336 each
+            N(0, 0.02).
   backward  dX = (dY @ W^T) * gelu_tanh'(preact), column sums of dX.
             dY 8192x4096 N(0,1); W 16384x4096 N(0, 0.02); preact 8192x16384
             N(0,1).
 
-Draw order per workload: A, B, bias, residual / preact.  Each tensor is drawn
+Draw order per workload: A, B, bias, residual / preact, B2.  Each tensor is drawn
 in fp32 with ``torch.randn`` from one generator seeded with 1000 + index,
 scaled, then cast to bf16 (round to nearest even); bias stays fp32.
 """
@@ -49,11 +52,12 @@ class Workload:
     aux_std: float = 1.0
     alpha: float = 1.0
     fp8_scale: float = 1.0
+    dual: bool = False   # B holds gate columns, B2 the matching up columns (N/2 each)
     notes: str = ""
 
     @property
     def n_out(self) -> int:
-        return self.N // 2 if any(op.startswith("pair_swiglu") for op in self.program) else self.N
+        return self.N // 2 if any(op.startswith("pair_") for op in self.program) else self.N
 
     @property
     def flops(self) -> int:
@@ -86,6 +90,9 @@ WORKLOADS = {
     "downproj": Workload("downproj", 3, 16384, 4096, 14336, "kn",
                          ("residual", "store_bf16", "row_rms:1e-6"),
                          a_std=1 / math.sqrt(14336), b_std=0.02, aux="residual"),
+    "swiglu2w": Workload("swiglu2w", 5, 8192, 28672, 4096, "kn",
+                         ("pair_swiglu:128", "store_bf16"),
+                         a_std=1.0, b_std=0.02, dual=True),
     "backward": Workload("backward", 4, 8192, 16384, 4096, "nk",
                          ("gelu_tanh_grad", "store_bf16", "col_sum"),
                          a_std=1.0, b_std=0.02, aux="preact"),
@@ -97,11 +104,12 @@ BY_INDEX = {w.index: w for w in WORKLOADS.values()}
 @dataclass
 class Inputs:
     A: torch.Tensor                 # M x K bf16
-    B: torch.Tensor                 # K x N or N x K bf16
+    B: torch.Tensor                 # K x N or N x K bf16 (N/2 columns with a B2)
     bias: Optional[torch.Tensor]    # fp32, length = columns where the bias op sits
     aux: Optional[torch.Tensor]     # M x n_out bf16 (residual or preact)
     alpha: float
     fp8_scale: float
+    B2: Optional[torch.Tensor] = None  # second weight operand, B's shape
     extra: dict = field(default_factory=dict)
 
 
@@ -110,7 +118,7 @@ def _bias_len(w: Workload) -> int:
     if "bias" not in prog:
         return 0
     ib = prog.index("bias")
-    ip = next((i for i, op in enumerate(prog) if op.startswith("pair_swiglu")), None)
+    ip = next((i for i, op in enumerate(prog) if op.startswith("pair_")), None)
     return w.N if (ip is None or ib < ip) else w.N // 2
 
 
@@ -125,11 +133,13 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs
         return t.to(dtype)
 
     A = draw((w.M, w.K), w.a_std)
-    B = draw((w.K, w.N) if w.b_layout == "kn" else (w.N, w.K), w.b_std)
+    nbc = w.N // 2 if w.dual else w.N
+    B = draw((w.K, nbc) if w.b_layout == "kn" else (nbc, w.K), w.b_std)
     nb = _bias_len(w)
     bias = draw((nb,), w.bias_std, torch.float32) if nb else None
     aux = draw((w.M, w.n_out), w.aux_std) if w.aux else None
-    return Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale)
+    B2 = draw(tuple(B.shape), w.b_std) if w.dual else None
+    return Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale, B2=B2)
 
 
 def bf16_bits(t: torch.Tensor):

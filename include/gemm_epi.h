@@ -19,7 +19,8 @@
  *  - alpha given as a host scalar, bias, activation and an AMAX reduction in
  *    the same kernel for the next FP8 quantisation: "Huong dan su dung NVIDIA
  *    cuDNN Graph API" (aihot.vn), batched matmul epilogue paragraph.
- *  - SwiGLU out = up * silu(gate): Superoptimizer, section 7 "SwiGLU".
+ *  - SwiGLU out = up * silu(gate): Superoptimizer, section 7 "SwiGLU"; the
+ *    RMSNorm-MLP's out = up * gate on rows scaled by S: section 10.
  *  - RMSNorm S = 1/sqrt(mean(x^2) + eps) and the row-broadcast rewrite
  *    (X*S)@W = (X@W)*S: Superoptimizer, sections 3 and 9 "RMSNorm".
  *  - a small set of composable epilogue primitives (scaling, reductions,
@@ -45,7 +46,8 @@
  *  - A: M x K bf16, row stride lda >= K.
  *  - B: GEMM_EPI_B_KN: K x N bf16, row stride ldb >= N;
  *       GEMM_EPI_B_NK: N x K bf16 (B = W^T for a weight W stored N x K),
- *       row stride ldb >= K.
+ *       row stride ldb >= K.  With GEMM_EPI_B_DUAL, B and B2 each hold N/2
+ *       columns (K x N/2, or N/2 x K), both with row stride ldb.
  *  - Output columns: N_out = N, or N/2 after GEMM_EPI_OP_PAIR_SWIGLU.
  *  - C: M x N_out bf16, row stride ldc >= N_out.  C8: M x N_out e4m3 bytes,
  *    row stride ldc8 >= N_out (bytes).
@@ -94,8 +96,15 @@ typedef enum gemm_epi_status {
 } gemm_epi_status;
 
 typedef enum gemm_epi_b_layout {
-    GEMM_EPI_B_KN = 0, /* B stored K x N row-major (N contiguous) */
-    GEMM_EPI_B_NK = 1  /* B stored N x K row-major (K contiguous), i.e. W^T */
+    GEMM_EPI_B_KN = 0,   /* B stored K x N row-major (N contiguous) */
+    GEMM_EPI_B_NK = 1,   /* B stored N x K row-major (K contiguous), i.e. W^T */
+    /* Flag OR-ed onto KN or NK: two weight operands.  B and args.B2 each hold
+     * N/2 columns (same layout and ldb); accumulator column n comes from B
+     * column (n/256)*128 + n%128 when (n/128) is even and from B2's same
+     * column when it is odd.  N % 256 == 0.  With a pair op of group 128 this
+     * is out = f(X@B) * (X@B2): SwiGLU with separate W_gate (B) and W_up (B2)
+     * sharing each A tile (Superoptimizer, section 7). */
+    GEMM_EPI_B_DUAL = 16
 } gemm_epi_b_layout;
 
 /*
@@ -112,7 +121,7 @@ typedef enum gemm_epi_op_code {
     GEMM_EPI_OP_ACT_RELU = 6,           /* y = max(y, 0)                                    */
     GEMM_EPI_OP_ACT_SILU = 7,           /* y = y * sigmoid(y)                               */
     GEMM_EPI_OP_PAIR_SWIGLU = 8,        /* y'[m,j] = silu(y[m,gate(j)]) * y[m,up(j)];
-                                           i0 = group g in {1,2,4,8,16,32} (0 means 1):
+                                           i0 = group g in {1,2,4,8,16,32,128} (0 means 1):
                                            gate(j) = (j/g)*2g + j%g, up(j) = gate(j) + g;
                                            g = 1 is even = gate, odd = up.  N_out = N/2.  */
     GEMM_EPI_OP_MUL_GELU_TANH_GRAD = 9, /* y = y * gelu_tanh'(preact[m, n]) (args.preact)    */
@@ -121,7 +130,10 @@ typedef enum gemm_epi_op_code {
     GEMM_EPI_OP_STORE_E4M3 = 12,        /* C8[m, n] = e4m3_rne_satfinite(y * args.fp8_scale) */
     GEMM_EPI_OP_ROW_RMS_RSQRT = 13,     /* row_out[m] = 1/sqrt(mean_n(v^2) + f0), f0 = eps;
                                            v = bf16_rne(y) when i0 == 0, v = y when i0 == 1 */
-    GEMM_EPI_OP_COL_SUM = 14            /* col_out[n] = sum over m of y                      */
+    GEMM_EPI_OP_COL_SUM = 14,           /* col_out[n] = sum over m of y                      */
+    GEMM_EPI_OP_PAIR_MUL = 15           /* y'[m,j] = y[m,gate(j)] * y[m,up(j)]: the RMSNorm-MLP's
+                                           plain up * gate; same groups and N_out as
+                                           PAIR_SWIGLU, at most one pair op per program      */
 } gemm_epi_op_code;
 
 typedef struct gemm_epi_op {
@@ -161,6 +173,7 @@ typedef struct gemm_epi_args {
     size_t workspace_bytes;
     uint32_t timeout_ms;      /* bound of every in-kernel wait; 0 = 2000 ms */
     uint32_t debug_flags;     /* 0 in normal use; GEMM_EPI_DEBUG_* for tests */
+    const void *B2;           /* second weight operand with GEMM_EPI_B_DUAL, bf16 */
 } gemm_epi_args;
 
 /* Test hook: the producer skips the first operand load of the first CTA so

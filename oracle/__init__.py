@@ -6,7 +6,7 @@ library and its Python binding never import it, and it imports nothing from
 them: inputs arrive as numpy arrays of bf16 bit patterns (uint16) and fp32.
 
 The program is a list of op names, optionally with one numeric argument:
-``alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g],
+``alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
 gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
 row_rms_unrounded[:eps], col_sum``.
 """
@@ -29,7 +29,7 @@ class _Problem(ctypes.Structure):
         ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
         ("b_is_nk", ctypes.c_int),
         ("A", ctypes.c_void_p), ("lda", ctypes.c_int64),
-        ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+        ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("B2", ctypes.c_void_p),
         ("alpha", ctypes.c_double),
         ("bias", ctypes.c_void_p), ("row_scale", ctypes.c_void_p),
         ("residual", ctypes.c_void_p), ("preact", ctypes.c_void_p),
@@ -92,6 +92,8 @@ class Problem:
 
     A: M x K bf16 bits (uint16), row-major with row stride ``A.shape[1]``.
     B: K x N bf16 bits when ``b_is_nk`` is False, else N x K.
+    B2: optional second weight operand of B's shape; the accumulator then
+    has 2 x B's columns, alternating between B and B2 in blocks of 128.
     """
     A: np.ndarray
     B: np.ndarray
@@ -103,15 +105,21 @@ class Problem:
     residual: Optional[np.ndarray] = None
     preact: Optional[np.ndarray] = None
     fp8_scale: float = 1.0
+    B2: Optional[np.ndarray] = None
 
     def _c(self):
         A = _u16(self.A)
         B = _u16(self.B)
         M, K = A.shape
         N = B.shape[0] if self.b_is_nk else B.shape[1]
+        B2 = _u16(self.B2)
+        if B2 is not None:
+            if B2.shape != B.shape:
+                raise ValueError("B2 must have B's shape")
+            N *= 2
         if (B.shape[1] if self.b_is_nk else B.shape[0]) != K:
             raise ValueError("A and B disagree on K")
-        keep = [A, B]
+        keep = [A, B, B2]
         bias = _f32(self.bias)
         rs = _f32(self.row_scale)
         res = _u16(self.residual)
@@ -122,7 +130,7 @@ class Problem:
         prog = ",".join(self.program).encode()
         keep.append(prog)
         p = _Problem(M, N, K, 1 if self.b_is_nk else 0,
-                     A.ctypes.data, A.shape[1], B.ctypes.data, B.shape[1],
+                     A.ctypes.data, A.shape[1], B.ctypes.data, B.shape[1], _ptr(B2),
                      float(self.alpha), _ptr(bias), _ptr(rs), _ptr(res), _ptr(pre),
                      ld_aux, float(self.fp8_scale), prog)
         return p, keep

@@ -22,7 +22,8 @@
  *    the next FP8 quantisation: "Huong dan su dung NVIDIA cuDNN Graph API"
  *    (aihot.vn), the batched matmul epilogue paragraph.
  *  - SwiGLU out = up * silu(gate), silu(x) = x * sigmoid(x): Superoptimizer,
- *    section 7 "SwiGLU".
+ *    section 7 "SwiGLU"; the RMSNorm-MLP's plain out = up * gate:
+ *    Superoptimizer, section 10 "RMSNorm-MLP".
  *  - RMSNorm scale S = 1 / sqrt(mean(x^2) + eps) and the row-broadcast rewrite
  *    (X*S)@W = (X@W)*S: Superoptimizer, sections 3 and 9 "RMSNorm".
  *  - scaling, reductions, pairwise transforms and accumulation applied to the
@@ -33,8 +34,9 @@
  *  - GELU is the tanh approximation 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715
  *    x^3))), evaluated as x * sigmoid(2u); its derivative is
  *    s + 2 x s (1 - s) sqrt(2/pi) (1 + 3*0.044715 x^2), s = sigmoid(2u).
- *  - pair_swiglu(g): output column j takes gate from accumulator column
- *    (j/g)*2g + j%g and up from (j/g)*2g + g + j%g; g = 1 is even/odd.
+ *  - pair_swiglu(g) / pair_mul(g): output column j takes gate from
+ *    accumulator column (j/g)*2g + j%g and up from (j/g)*2g + g + j%g; g = 1
+ *    is even/odd.
  *  - e4m3 is OCP FP8 E4M3FN (bias 7, max 448, no infinities); quantisation is
  *    round-to-nearest-even of value*scale, saturated to +-448, NaN kept.
  *  - row_rms averages the squares of the bf16-rounded values (what the next
@@ -163,7 +165,7 @@ double oracle_silu(double x) { return x * sigmoid(x); }
 
 enum {
     O_ALPHA, O_BIAS, O_ROW_SCALE, O_RESIDUAL, O_GELU, O_RELU, O_SILU, O_PAIR,
-    O_GELU_GRAD, O_AMAX, O_STORE_BF16, O_STORE_E4M3, O_ROW_RMS, O_COL_SUM
+    O_PAIR_MUL, O_GELU_GRAD, O_AMAX, O_STORE_BF16, O_STORE_E4M3, O_ROW_RMS, O_COL_SUM
 };
 
 typedef struct { int code; double f; int i; } oop;
@@ -179,7 +181,7 @@ static int parse_program(const char *s, oop *ops, int *n_out)
     static const struct { const char *name; int code; int mode; } names[] = {
         {"alpha", O_ALPHA, 0}, {"bias", O_BIAS, 0}, {"row_scale", O_ROW_SCALE, 0},
         {"residual", O_RESIDUAL, 0}, {"gelu_tanh", O_GELU, 0}, {"relu", O_RELU, 0},
-        {"silu", O_SILU, 0}, {"pair_swiglu", O_PAIR, 0},
+        {"silu", O_SILU, 0}, {"pair_swiglu", O_PAIR, 0}, {"pair_mul", O_PAIR_MUL, 0},
         {"gelu_tanh_grad", O_GELU_GRAD, 0}, {"amax", O_AMAX, 0},
         {"store_bf16", O_STORE_BF16, 0}, {"store_e4m3", O_STORE_E4M3, 0},
         {"row_rms", O_ROW_RMS, 0}, {"row_rms_unrounded", O_ROW_RMS, 1},
@@ -207,8 +209,8 @@ static int parse_program(const char *s, oop *ops, int *n_out)
         ops[n].f = f;
         ops[n].i = code == O_ROW_RMS ? mode : (int)f;
         /* defaults */
-        if (code == O_PAIR && !has_arg) ops[n].i = 1;           /* group g */
-        if (code == O_PAIR && ops[n].i < 1) return -1;
+        if ((code == O_PAIR || code == O_PAIR_MUL) && !has_arg) ops[n].i = 1; /* group g */
+        if ((code == O_PAIR || code == O_PAIR_MUL) && ops[n].i < 1) return -1;
         if (code == O_ROW_RMS && !has_arg) ops[n].f = 1e-6;     /* eps */
         ++n;
     }
@@ -225,17 +227,25 @@ static double a_at(const oracle_problem *p, int64_t m, int64_t k)
     return oracle_bf16_to_double(p->A[m * p->lda + k]);
 }
 
+/* Accumulator column n.  With a second weight operand B2 the columns
+ * alternate in blocks of 128: block 2i is B's columns [128i, 128i+128),
+ * block 2i+1 is B2's same columns. */
 static double b_at(const oracle_problem *p, int64_t k, int64_t n)
 {
-    return p->b_is_nk ? oracle_bf16_to_double(p->B[n * p->ldb + k])
-                      : oracle_bf16_to_double(p->B[k * p->ldb + n]);
+    const uint16_t *src = p->B;
+    if (p->B2) {
+        if ((n / 128) % 2) src = p->B2;
+        n = (n / 256) * 128 + n % 128;
+    }
+    return p->b_is_nk ? oracle_bf16_to_double(src[n * p->ldb + k])
+                      : oracle_bf16_to_double(src[k * p->ldb + n]);
 }
 
 /* One whole accumulator row, i-k-j order for the K x N layout. */
 static void acc_row(const oracle_problem *p, int64_t m, double *acc)
 {
     for (int64_t n = 0; n < p->N; ++n) acc[n] = 0.0;
-    if (!p->b_is_nk) {
+    if (!p->b_is_nk && !p->B2) {
         for (int64_t k = 0; k < p->K; ++k) {
             double a = a_at(p, m, k);
             const uint16_t *brow = p->B + k * p->ldb;
@@ -276,7 +286,7 @@ typedef struct {
 static int find_pair(const oop *ops, int n)
 {
     for (int i = 0; i < n; ++i)
-        if (ops[i].code == O_PAIR) return i;
+        if (ops[i].code == O_PAIR || ops[i].code == O_PAIR_MUL) return i;
     return -1;
 }
 
@@ -314,7 +324,7 @@ static void run_elem(const oracle_problem *p, const oop *ops, int nops, int64_t 
             yg = apply_elementwise(p, &ops[i], yg, m, cg);
             yu = apply_elementwise(p, &ops[i], yu, m, cu);
         }
-        y = oracle_silu(yg) * yu;
+        y = ops[ip].code == O_PAIR ? oracle_silu(yg) * yu : yg * yu;
         first_post = ip + 1;
     } else {
         y = acc_a;

@@ -21,6 +21,7 @@ typedef struct {
     int64_t lda;
     const uint16_t *B;           /* bf16 bit patterns */
     int64_t ldb;
+    const uint16_t *B2;          /* second weight operand or NULL (same layout, ldb) */
     double alpha;                /* op "alpha" */
     const float *bias;           /* op "bias": one value per column at its point of use */
     const float *row_scale;      /* op "row_scale": M values */

@@ -98,17 +98,18 @@ def oracle_problem(w: synth.Workload, inp: synth.Inputs) -> oracle.Problem:
         A=bits(inp.A), B=bits(inp.B), program=prog, b_is_nk=(w.b_layout == "nk"),
         alpha=inp.alpha, bias=None if inp.bias is None else inp.bias.detach().cpu().numpy(),
         residual=aux if w.aux == "residual" else None,
-        preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale)
+        preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
+        B2=bits(inp.B2) if inp.B2 is not None else None)
 
 
 def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
-    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual)
     out = api.allocate_outputs(plan, inp.A.device)
     scratch = None
     if unfused:
         scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=inp.A.device)
     api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
-                    bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, **kw)
+                    bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, B2=inp.B2, **kw)
     torch.cuda.synchronize()
     status = plan.query_status(out.workspace)
     assert status == 0, "kernel status %d" % status

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_layouts_match_header(lib):
     assert ctypes.sizeof(N.gemm_epi_op) == 12
     assert ctypes.sizeof(N.gemm_epi_desc) == 8 * 8 + 4 + 4 + 8
-    assert ctypes.sizeof(N.gemm_epi_args) == 2 * 8 + 2 * 4 + 10 * 8 + 8 + 2 * 4
+    assert ctypes.sizeof(N.gemm_epi_args) == 2 * 8 + 2 * 4 + 10 * 8 + 8 + 2 * 4 + 8
 
 
 def test_version_and_status_strings(lib):
@@ -112,7 +112,14 @@ def test_create_accepts_programs(lib, program):
     (dict(program=("residual", "store_bf16"), ld_aux=12), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(N_=0, program=("row_rms",)), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(program=("store_bf16",), n_ops=17), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(layout=N.GEMM_EPI_B_KN | N.GEMM_EPI_B_DUAL, N_=384, program=("pair_swiglu:128", "store_bf16"),
+          ldb=192), N.GEMM_EPI_ERR_INVALID_VALUE),                       # N % 256
+    (dict(layout=N.GEMM_EPI_B_KN | N.GEMM_EPI_B_DUAL, program=("pair_swiglu", "store_bf16"), ldb=256),
+     N.GEMM_EPI_ERR_INVALID_VALUE),                                      # group must be 128
+    (dict(program=("bias", "pair_swiglu:128", "store_bf16")), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(layout=N.GEMM_EPI_B_NK | 32, program=("store_bf16",)), N.GEMM_EPI_ERR_INVALID_VALUE),
 ])
+
 def test_create_rejects(lib, kw, status):
     s, h = create(lib, **kw)
     assert s == status, (s, lib.gemm_epi_last_error())
@@ -153,3 +160,15 @@ def test_workspace_grows_with_row_tiles(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         N.load(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("layout", [N.GEMM_EPI_B_KN, N.GEMM_EPI_B_NK])
+def test_create_accepts_two_weight_programs(lib, layout):
+    for prog in (("pair_swiglu:128", "store_bf16"), ("row_scale", "pair_mul:128", "store_bf16"),
+                 ("store_bf16",)):
+        s, h = create(lib, N_=512, program=prog, layout=layout | N.GEMM_EPI_B_DUAL,
+                      ldb=256 if layout == N.GEMM_EPI_B_KN else 128)
+        assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
+        pair = any(p.startswith("pair") for p in prog)
+        assert lib.gemm_epi_out_cols(h) == (256 if pair else 512)
+        lib.gemm_epi_destroy(h)

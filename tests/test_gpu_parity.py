@@ -41,6 +41,7 @@ SMALL_SHAPES = [
     ("fp8", 257, 528, 264),         # FP8 store + AMAX, 16-column N tail, K tail of 8
     ("downproj", 384, 1000, 328),   # residual + row RMS across 4 N tiles
     ("backward", 200, 776, 192),    # B stored N x K, gelu' + column sums
+    ("swiglu2w", 300, 768, 200),    # separate gate / up weights, 384 output columns
 ]
 
 
@@ -74,7 +75,7 @@ def unfused_oracle(w, inp):
     return p
 
 
-@pytest.mark.parametrize("name,M,N,K", SMALL_SHAPES[1:])
+@pytest.mark.parametrize("name,M,N,K", [s for s in SMALL_SHAPES[1:] if s[0] != "swiglu2w"])
 def test_small_unfused_baseline(name, M, N, K):
     w = small(name, M, N, K)
     inp = synth.make_inputs(w, DEV)
@@ -96,6 +97,9 @@ def test_small_unfused_baseline(name, M, N, K):
     (("pair_swiglu:32", "relu", "store_bf16", "col_sum"), "nk"),
     (("residual", "gelu_tanh", "store_bf16", "store_e4m3", "row_rms_unrounded:1e-5"), "nk"),
     (("gelu_tanh_grad", "amax", "store_bf16", "col_sum", "row_rms"), "kn"),
+    (("row_scale", "pair_mul", "store_bf16"), "kn"),
+    (("row_scale", "pair_swiglu", "store_bf16"), "kn"),
+    (("pair_mul:8", "amax", "store_bf16"), "nk"),
 ])
 def test_program_variants(program, layout, variant):
     aux = "residual" if "residual" in program else ("preact" if "gelu_tanh_grad" in program else None)
@@ -114,6 +118,81 @@ def test_program_variants(program, layout, variant):
     compare_rows(w, inp, out, oracle_p=p)
     if out.col_out is not None:
         compare_cols(w, inp, out, list(range(w.n_out)), oracle_p=p)
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("program", [("pair_swiglu:128", "store_bf16"),
+                                     ("row_scale", "pair_mul:128", "store_bf16"),
+                                     ("alpha", "pair_swiglu:128", "amax", "store_bf16", "col_sum")])
+def test_two_weight_programs(program, layout, variant):
+    """Separate gate / up weights (GEMM_EPI_B_DUAL): out = f(X@B) * (X@B2)."""
+    w = synth.Workload("two_weight", 13, 260, 1280, 136, layout, program, a_std=0.3, b_std=0.3,
+                       alpha=0.75, dual=True)
+    inp = synth.make_inputs(w, DEV, seed=31)
+    row_scale = torch.rand(w.M, device=DEV) + 0.5
+    plan = api.Plan(w.M, w.N, w.K, program, b_layout=layout, dual=True)
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, row_scale=row_scale, B2=inp.B2,
+                    debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    p = oracle_problem(w, inp)
+    p.row_scale = row_scale.cpu().numpy()
+    compare_rows(w, inp, out, oracle_p=p)
+    if out.col_out is not None:
+        compare_cols(w, inp, out, list(range(w.n_out)), oracle_p=p)
+
+
+@pytest.mark.parametrize("pair", ["pair_mul", "pair_swiglu"])
+def test_rmsnorm_mlp_chain(pair):
+    """The RMSNorm-MLP chain of the Superoptimizer page (section 10) without a
+    separate scale kernel: a down-projection emits out = residual + X@W1 and
+    S = 1/sqrt(mean(out^2) + eps) from its epilogue; the next GEMM consumes
+    out with S as a row scale, (out*S)@W2 = (out@W2)*S, and pairs gate/up
+    (plain product, or SwiGLU).  Each stage's oracle reads the oracle's own
+    stage-1 results, never the GPU's."""
+    g = torch.Generator(device=DEV).manual_seed(21)
+    M, K1, H, N2 = 384, 512, 1024, 1536
+    X = (torch.randn(M, K1, generator=g, device=DEV) / K1 ** 0.5).to(torch.bfloat16)
+    W1 = (torch.randn(K1, H, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+    R = torch.randn(M, H, generator=g, device=DEV).to(torch.bfloat16)
+    W2 = (torch.randn(H, N2, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+    prog1 = ["residual", "store_bf16", "row_rms:1e-6"]
+    prog2 = ["row_scale", pair, "store_bf16"]
+    p1 = api.Plan(M, H, K1, prog1)
+    o1 = api.allocate_outputs(p1, DEV)
+    api.run_program(p1, X, W1, o1, aux=R)
+    p2 = api.Plan(M, N2, H, prog2)
+    o2 = api.allocate_outputs(p2, DEV)
+    api.run_program(p2, o1.C, W2, o2, row_scale=o1.row_out)
+    torch.cuda.synchronize()
+    assert p1.query_status(o1.workspace) == 0 and p2.query_status(o2.workspace) == 0
+    r1 = oracle.Problem(bits(X), bits(W1), prog1, residual=bits(R)).rows()
+    check_rows(o1.row_out.cpu().numpy(), r1["row_stat"])
+    S = r1["row_stat"].astype(np.float32)
+    r2 = oracle.Problem(r1["c_bf16"], bits(W2), prog2, row_scale=S).rows()
+    # Stage 1 rounds out to bf16 from fp32 on the GPU and from fp64 in the
+    # oracle, so a few stage-2 inputs differ by one bf16 ulp.  Carried through
+    # the GEMM (|W2|), the row scale and the pair op (|silu'| <= 1.1), that
+    # bounds the extra stage-2 difference per element; it is added to the
+    # bf16 tolerance of a single stage.
+    Xr = oracle.bf16_bits_to_f64(r1["c_bf16"])
+    with np.errstate(divide="ignore"):
+        ulp = np.where(Xr != 0, 2.0 ** (np.floor(np.log2(np.abs(Xr))) - 7), 0.0)
+    E = (ulp @ np.abs(oracle.bf16_bits_to_f64(bits(W2)))) * S[:, None]  # M x N2 accumulator bound
+    acc = oracle.Problem(r1["c_bf16"], bits(W2), ["row_scale"], row_scale=S).rows()["y"]
+    ag, au, Eg, Eu = acc[:, 0::2], acc[:, 1::2], E[:, 0::2], E[:, 1::2]
+    if pair == "pair_mul":
+        fg, dfg = np.abs(ag), 1.0
+    else:
+        fg, dfg = np.abs(ag / (1 + np.exp(-ag))), 1.1
+    prop = dfg * Eg * np.abs(au) + fg * Eu + dfg * Eg * Eu
+    g2 = oracle.bf16_bits_to_f64(bits(o2.C))
+    rms = float(np.sqrt(np.mean(r2["y"] ** 2)))
+    bound = 2e-2 * np.maximum(np.abs(r2["y"]), 1e-2 * rms) + prop
+    bad = np.abs(g2 - r2["y"]) > bound
+    assert not bad.any(), "chain output: %d of %d outside the propagated bound" % (int(bad.sum()), bad.size)
 
 
 # ------------------------------------------------------------ exact pins on the GPU
@@ -280,7 +359,7 @@ def test_graph_capture_replay_matches_eager():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = ["tiny", "swiglu", "fp8", "downproj", "backward"]
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w"]
 
 
 @pytest.mark.parametrize("name", FULL)

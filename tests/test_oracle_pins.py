@@ -217,7 +217,7 @@ def brute_force(A, B, b_is_nk, program, alpha=1.0, bias=None, row_scale=None, au
             return y * gelu_grad(f64(aux)[m, n])
         raise KeyError(op)
 
-    pair = [i for i, op in enumerate(program) if op.startswith("pair_swiglu")]
+    pair = [i for i, op in enumerate(program) if op.startswith("pair_")]
     nout = N // 2 if pair else N
     out = {"y": np.zeros((M, nout)), "amax": 0.0, "col": np.zeros(nout), "row": np.zeros(M)}
     for m in range(M):
@@ -230,7 +230,7 @@ def brute_force(A, B, b_is_nk, program, alpha=1.0, bias=None, row_scale=None, au
                 yg, yu = acc(m, cg), acc(m, cu)
                 for op in program[:ip]:
                     yg, yu = ew(op, yg, m, cg), ew(op, yu, m, cu)
-                y = silu(yg) * yu
+                y = (silu(yg) if program[ip].startswith("pair_swiglu") else yg) * yu
                 rest = program[ip + 1:]
             else:
                 y = acc(m, j)
@@ -262,6 +262,8 @@ PROGRAMS = [
     (("residual", "store_bf16", "row_rms:1e-6"), "kn"),
     (("gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
     (("row_scale", "silu", "store_bf16"), "nk"),
+    (("row_scale", "pair_mul", "store_bf16"), "kn"),
+    (("alpha", "pair_mul:2", "amax", "store_bf16"), "nk"),
 ]
 
 
@@ -372,3 +374,23 @@ def test_bad_program_rejected():
     A = rand_bf16((2, 2))
     with pytest.raises(ValueError):
         Problem(A, A, ["no_such_op"]).rows()
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("pair", ["pair_swiglu:128", "pair_mul:128"])
+def test_two_weight_pairs_match_numpy(layout, pair):
+    """With a second weight operand and pair group 128, out = f(A@W_gate) *
+    (A@W_up) (Superoptimizer, section 7: gate = X @ W_gate, up = X @ W_up)."""
+    M, K, H = 5, 24, 384
+    A = rand_bf16((M, K))
+    Wg = rand_bf16((K, H) if layout == "kn" else (H, K))
+    Wu = rand_bf16((K, H) if layout == "kn" else (H, K))
+    p = Problem(A, Wg, [pair, "store_bf16"], b_is_nk=(layout == "nk"), B2=Wu)
+    assert p.out_cols() == H
+    y = p.rows()["y"]
+    G = f64(A) @ (f64(Wg) if layout == "kn" else f64(Wg).T)
+    U = f64(A) @ (f64(Wu) if layout == "kn" else f64(Wu).T)
+    f = G / (1 + np.exp(-G)) if pair.startswith("pair_swiglu") else G
+    np.testing.assert_allclose(y, f * U, rtol=1e-12, atol=1e-14)
+    cols = p.cols([0, 127, 128, 383])
+    np.testing.assert_allclose(cols["y"], y[:, [0, 127, 128, 383]], rtol=1e-15)
