@@ -66,7 +66,10 @@ class Plan:
 
     def __init__(self, M: int, N_: int, K: int, program: Sequence[str], b_layout: str = "kn",
                  lda: Optional[int] = None, ldb: Optional[int] = None, ldc: Optional[int] = None,
-                 ldc8: Optional[int] = None, ld_aux: Optional[int] = None, dual: bool = False):
+                 ldc8: Optional[int] = None, ld_aux: Optional[int] = None, dual: bool = False,
+                 batch: int = 1, batch_stride_a: Optional[int] = None,
+                 batch_stride_b: Optional[int] = None, batch_stride_c: Optional[int] = None,
+                 batch_stride_c8: Optional[int] = None, batch_stride_aux: Optional[int] = None):
         self.lib = N.load()
         self.program = list(program)
         self.M, self.N, self.K = M, N_, K
@@ -86,6 +89,15 @@ class Plan:
         self.dual = dual
         d.n_ops = len(program)
         d.ops = ctypes.cast(self._ops, ctypes.POINTER(N.gemm_epi_op))
+        # Batched: tight packing by default; a stride of 0 shares A or B.
+        d.batch = batch
+        b_rows = K if b_layout == "kn" else b_cols
+        d.batch_stride_a = M * d.lda if batch_stride_a is None else batch_stride_a
+        d.batch_stride_b = b_rows * d.ldb if batch_stride_b is None else batch_stride_b
+        d.batch_stride_c = M * d.ldc if batch_stride_c is None else batch_stride_c
+        d.batch_stride_c8 = M * d.ldc8 if batch_stride_c8 is None else batch_stride_c8
+        d.batch_stride_aux = M * d.ld_aux if batch_stride_aux is None else batch_stride_aux
+        self.batch = batch
         self.desc = d
         h = N.gemm_epi_handle()
         N.check(self.lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)), self.lib)
@@ -146,16 +158,17 @@ def allocate_outputs(plan: Plan, device) -> Outputs:
     """Device buffers for every output the program writes (torch allocates)."""
     prog = [op.partition(":")[0] for op in plan.program]
     o = Outputs()
+    lead = (plan.batch,) if plan.batch > 1 else ()
     if "store_bf16" in prog:
-        o.C = torch.empty((plan.M, plan.n_out), dtype=torch.bfloat16, device=device)
+        o.C = torch.empty(lead + (plan.M, plan.n_out), dtype=torch.bfloat16, device=device)
     if "store_e4m3" in prog:
-        o.C8 = torch.empty((plan.M, plan.n_out), dtype=torch.uint8, device=device)
+        o.C8 = torch.empty(lead + (plan.M, plan.n_out), dtype=torch.uint8, device=device)
     if "amax" in prog:
         o.amax = torch.empty(1, dtype=torch.float32, device=device)
     if any(p.startswith("row_rms") for p in prog):
-        o.row_out = torch.empty(plan.M, dtype=torch.float32, device=device)
+        o.row_out = torch.empty(lead + (plan.M,), dtype=torch.float32, device=device)
     if "col_sum" in prog:
-        o.col_out = torch.empty(plan.n_out, dtype=torch.float32, device=device)
+        o.col_out = torch.empty(lead + (plan.n_out,), dtype=torch.float32, device=device)
     o.workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=device)
     return o
 

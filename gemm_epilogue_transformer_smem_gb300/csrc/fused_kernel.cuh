@@ -128,6 +128,9 @@ struct KernelParams {
   int32_t group_m;
   int32_t b_kn;  // 1: B stored K x N (MN-major operand)
   int32_t dual;  // 1: accumulator columns alternate between B and B2 in 128-column blocks
+  int32_t a_batched, b_batched;  // operand advances with the batch (else shared)
+  int32_t row_blocks;            // row counters per batch
+  int64_t bs_c, bs_c8, bs_aux;   // batch strides for direct accesses (elements; bytes for C8)
   uint32_t idesc;
   uint32_t flags;
   int32_t n_ops;
@@ -247,7 +250,12 @@ __host__ __device__ constexpr uint32_t static_flags() {
 
 // ------------------------------------------------------------------ helpers
 
-__device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& mb, int& nb) {
+// Tile t of the persistent walk: batch b, then groups of group_m M-tiles
+// walked along N.
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& b, int& mb, int& nb) {
+  const int per_batch = p.num_m_tiles * p.num_n_tiles;
+  b = t / per_batch;
+  t -= b * per_batch;
   const int per_group = p.group_m * p.num_n_tiles;
   const int g = t / per_group;
   const int first_m = g * p.group_m;
@@ -428,10 +436,10 @@ __device__ __forceinline__ void pair_combine(const float (&a)[64], float (&out)[
 
 // This thread's 32 auxiliary bf16 values of row m, columns col0.. (zeros
 // outside the tensor), straight from global memory.
-__device__ __forceinline__ void load_aux_row(uint4 (&w)[4], const KernelParams& p, int m, bool row_ok,
-                                             int col0) {
+__device__ __forceinline__ void load_aux_row(uint4 (&w)[4], const KernelParams& p, const uint16_t* aux,
+                                             int m, bool row_ok, int col0) {
   if (row_ok && col0 + 32 <= p.n_out) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.aux + static_cast<int64_t>(m) * p.ld_aux + col0);
+    const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<int64_t>(m) * p.ld_aux + col0);
 #pragma unroll
     for (int q = 0; q < 4; ++q) w[q] = __ldg(src + q);
   } else {
@@ -439,7 +447,7 @@ __device__ __forceinline__ void load_aux_row(uint4 (&w)[4], const KernelParams& 
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int n = col0 + 2 * j;
-      const uint16_t* rowp = p.aux + static_cast<int64_t>(m) * p.ld_aux;
+      const uint16_t* rowp = aux + static_cast<int64_t>(m) * p.ld_aux;
       const uint32_t lo = (row_ok && n < p.n_out) ? rowp[n] : 0u;
       const uint32_t hi = (row_ok && n + 1 < p.n_out) ? rowp[n + 1] : 0u;
       h[j] = lo | (hi << 16);
@@ -537,8 +545,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued = 0, issued_parity = 0;  // per-stage bits, for the abort drain
       bool ok = true;
       for (int t = group; ok && t < p.num_tiles; t += num_groups) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
+        int bt, mb, nb;
+        tile_coords(p, t, bt, mb, nb);
+        const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;
         const int a_row = mb * TILE_M + rank * BLOCK_M;
         // B columns of this tile.  With two weight operands, tile nb covers
         // columns [nb*128, nb*128+128) of B (accumulator columns 0..127) and
@@ -558,34 +567,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
             if (CG == 1) {
               ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + L::B_STAGE_BYTES);
-              ptx::tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, a_row);
+              ptx::tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j) {
                   // with B2, boxes 0-1 come from B and 2-3 from B2
                   const bool second = p.dual && j >= 2;
                   const int col = p.dual ? b_col + (j & 1) * 64 : b_col + j * 64;
-                  ptx::tma_load_2d(sb + j * B_MN_BOX_BYTES, second ? &tm_b2 : &tm_b, fb, col, kb * BLOCK_K);
+                  ptx::tma_load_3d(sb + j * B_MN_BOX_BYTES, second ? &tm_b2 : &tm_b, fb, col, kb * BLOCK_K, zb);
                 }
               } else if (p.dual) {
                 // two 128-row K-major boxes, one per operand, stacked in the stage
-                ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, b_col);
-                ptx::tma_load_2d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * BLOCK_K, b_col);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, b_col, zb);
+                ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * BLOCK_K, b_col, zb);
               } else {
-                ptx::tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, b_col);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, b_col, zb);
               }
             } else {
               // Both CTAs' halves complete on the even CTA's full barrier,
               // which expects the bytes of the whole pair.
               const uint32_t fb0 = ptx::mapa_shared(fb, 0);
               if (rank == 0) ptx::mbar_arrive_expect_tx(fb, 2u * (A_STAGE_BYTES + L::B_STAGE_BYTES));
-              ptx::tma_load_2d_cg2(sa, &tm_a, fb0, kb * BLOCK_K, a_row);
+              ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * BLOCK_K, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j)
-                  ptx::tma_load_2d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K);
+                  ptx::tma_load_3d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K, zb);
               } else {
-                ptx::tma_load_2d_cg2(sb, tmb_own, fb0, kb * BLOCK_K, b_col);
+                ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * BLOCK_K, b_col, zb);
               }
             }
             issued |= 1u << stage;
@@ -698,8 +707,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 
     for (int t = group; ok && t < p.num_tiles; t += num_groups, ++local) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+      int bt, mb, nb;
+      tile_coords(p, t, bt, mb, nb);
+      const int64_t row_base = static_cast<int64_t>(bt) * p.M;  // this batch's rows in row_scale / row_out
+      const uint16_t* aux_b = p.aux ? p.aux + bt * p.bs_aux : nullptr;
+      uint16_t* c_b = p.c ? p.c + bt * p.bs_c : nullptr;
+      uint8_t* c8_b = p.c8 ? p.c8 + bt * p.bs_c8 : nullptr;
+      float* col_b = p.col_out ? p.col_out + static_cast<int64_t>(bt) * p.n_out : nullptr;
       const int blk = mb * CG + static_cast<int>(rank);  // this CTA's 128-row block
       const int m = blk * BLOCK_M + quad * 32 + lane;
       const bool row_ok = m < p.M;
@@ -708,12 +722,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int n0 = nb * tile_out_cols;       // first output column of the tile
       const int nacc0 = nb * BLOCK_N;          // first accumulator column
       const uint32_t buf = local & 1, use = local >> 1;
-      const float rs_m = (p.row_scale != nullptr && row_ok) ? __ldg(p.row_scale + m) : 0.0f;
+      const float rs_m = (p.row_scale != nullptr && row_ok) ? __ldg(p.row_scale + row_base + m) : 0.0f;
 
       // Residual / pre-activation rows are read straight into registers,
       // one chunk ahead of their use (each thread reads its own row).
       uint4 xa[4];
-      if (flags & F_AUX) load_aux_row(xa, p, m, row_ok, n0);
+      if (flags & F_AUX) load_aux_row(xa, p, aux_b, m, row_ok, n0);
 
       // All lanes wait; the outcome is made warp-uniform so that no lane
       // leaves while the others enter a warp-synchronous step.
@@ -795,7 +809,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               x[8 * q + 2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
             }
           }
-          if (c + 1 < chunks) load_aux_row(xa, p, m, row_ok, n0 + (c + 1) * CHUNK);
+          if (c + 1 < chunks) load_aux_row(xa, p, aux_b, m, row_ok, n0 + (c + 1) * CHUNK);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = 0.0f;
@@ -839,7 +853,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < 32; ++j) {
                   const int n = col0 + j;
                   if (n >= p.n_al && n < p.n_out)
-                    p.c[static_cast<int64_t>(m) * p.ldc + n] =
+                    c_b[static_cast<int64_t>(m) * p.ldc + n] =
                         static_cast<uint16_t>(ptx::pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
                 }
               }
@@ -866,7 +880,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < 32; ++j) {
                   const int n = col0 + j;
                   if (n >= p.n_al8 && n < p.n_out)
-                    p.c8[static_cast<int64_t>(m) * p.ldc8 + n] =
+                    c8_b[static_cast<int64_t>(m) * p.ldc8 + n] =
                         static_cast<uint8_t>(ptx::pack_e4m3x2(v[j] * s, 0.0f) & 0xFFu);
                 }
               }
@@ -884,7 +898,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) s[j] = row_ok ? v[j] : 0.0f;
               const float tot = warp_transpose_sum(s, lane);
-              if (slab_ok && col0 + lane < p.n_out) atomicAdd(p.col_out + col0 + lane, tot);
+              if (slab_ok && col0 + lane < p.n_out) atomicAdd(col_b + col0 + lane, tot);
               break;
             }
             default:
@@ -904,14 +918,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::fence_proxy_async_smem();  // generic smem writes before the async-proxy reads
           __syncwarp();
           if (lane == 0) {
-            if (slab_ok) {
-              if ((flags & F_STORE) && col0 < p.n_al)
-                ptx::tma_store_2d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0);
-              if ((flags & F_E8) && col0 < p.n_al8)
-                ptx::tma_store_2d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0);
+            const bool st_c = slab_ok && (flags & F_STORE) && col0 < p.n_al;
+            const bool st_8 = slab_ok && (flags & F_E8) && col0 < p.n_al8;
+            if (st_c) ptx::tma_store_3d(&tm_c, epi0 + eb * EPI_BUF_BYTES, col0, slab_row0, bt);
+            if (st_8) ptx::tma_store_3d(&tm_c8, e80 + (g % E8_BUFS) * E8_BUF_BYTES, col0, slab_row0, bt);
+            // At most the group of this chunk stays in flight, so the next
+            // chunk's buffers are free.  A chunk without stores commits no
+            // group and waits for every earlier read instead: a chunk past
+            // the output edge must not count as the group that frees a buffer.
+            if (st_c || st_8) {
+              ptx::bulk_commit_group();
+              ptx::bulk_wait_group_read<1>();
+            } else {
+              ptx::bulk_wait_group_read<0>();
             }
-            ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read<1>();  // the buffer of chunk g-1 is free again
           }
         }
         __syncwarp();
@@ -922,11 +942,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---- row statistics: partial sums, then the last arriving warp of
       // this row block turns them into 1/sqrt(mean + eps).
       if (flags & F_ROW) {
-        if (row_ok) atomicAdd(p.row_out + m, row_ss);
+        if (row_ok) atomicAdd(p.row_out + row_base + m, row_ss);
         __threadfence();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(p.row_counter + blk, 1u);
+        if (lane == 0) prev = atomicAdd(p.row_counter + static_cast<int64_t>(bt) * p.row_blocks + blk, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == static_cast<uint32_t>(NUM_EPI_WARPS * p.num_n_tiles - 1)) {
           __threadfence();
@@ -934,8 +954,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int r = lane; r < BLOCK_M; r += 32) {
             const int mm = blk * BLOCK_M + r;
             if (mm < p.M) {
-              const float ss = __ldcg(p.row_out + mm);
-              p.row_out[mm] = 1.0f / sqrtf(fmaf(ss, inv_n, p.rms_eps));
+              const float ss = __ldcg(p.row_out + row_base + mm);
+              p.row_out[row_base + mm] = 1.0f / sqrtf(fmaf(ss, inv_n, p.rms_eps));
             }
           }
         }

@@ -138,14 +138,21 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 3-D tiled map: x (contiguous), rows, batch.  `batch_bytes` == 0 means the
+// operand is shared across the batch (a batch extent of 1).
 gemm_epi_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                         CUtensorMapSwizzle sw, CUtensorMapL2promotion l2, const char* what) {
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CUtensorMapSwizzle sw, CUtensorMapL2promotion l2, const char* what,
+                         uint64_t batch = 1, uint64_t batch_bytes = 0) {
+  if (batch_bytes == 0) {
+    batch = 1;
+    batch_bytes = row_bytes * (outer > 0 ? outer : 1);
+  }
+  cuuint64_t dims[3] = {inner, outer, batch};
+  cuuint64_t strides[2] = {row_bytes, batch_bytes};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(GEMM_EPI_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
@@ -170,6 +177,7 @@ struct gemm_epi_plan {
   int64_t n_out = 0;
   int pair_at = -1, pair_g = 1, pair_silu = 1;
   bool dual = false;  // GEMM_EPI_B_DUAL: B columns alternate with B2 in 128-column blocks
+  int64_t batch = 1, row_blocks = 0;
   uint32_t flags = 0;
   bool uses_bias = false, uses_row_scale = false, uses_residual = false, uses_preact = false;
   float rms_eps = 0.0f;
@@ -284,11 +292,32 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 
   P.num_m_tiles = (d.M + ge::BLOCK_M - 1) / ge::BLOCK_M;
   P.num_n_tiles = (d.N + ge::BLOCK_N - 1) / ge::BLOCK_N;
-  if (P.num_m_tiles * P.num_n_tiles > LIM) return fail(GEMM_EPI_ERR_INVALID_VALUE, "too many tiles");
+  // Batch: 0 or 1 is a single problem; strides in elements (bytes for C8).
+  P.batch = d.batch <= 1 ? 1 : d.batch;
+  if (d.batch < 0 || P.batch > 65535) return fail(GEMM_EPI_ERR_INVALID_VALUE, "batch must be in [0, 65535]");
+  if (P.batch > 1) {
+    const int64_t b_rows = kn ? d.K : b_cols;
+    auto bad_stride = [&](int64_t st, int64_t need, int64_t mult, bool may_share) {
+      if (st == 0) return !may_share;
+      return st < need || st % mult != 0;
+    };
+    if (d.K > 0 && (bad_stride(d.batch_stride_a, d.M * d.lda, 8, true) ||
+                    bad_stride(d.batch_stride_b, b_rows * d.ldb, 8, true)))
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "A / B batch strides must be 0 (shared) or span a whole "
+                                              "operand, in multiples of 8 elements");
+    if ((P.flags & ge::F_STORE) && bad_stride(d.batch_stride_c, d.M * d.ldc, 8, false))
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "batch_stride_c must span M x ldc, a multiple of 8");
+    if ((P.flags & ge::F_E8) && bad_stride(d.batch_stride_c8, d.M * d.ldc8, 16, false))
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "batch_stride_c8 must span M x ldc8, a multiple of 16");
+    if ((P.flags & ge::F_AUX) && bad_stride(d.batch_stride_aux, d.M * d.ld_aux, 8, false))
+      return fail(GEMM_EPI_ERR_INVALID_VALUE, "batch_stride_aux must span M x ld_aux, a multiple of 8");
+  }
+  if (P.num_m_tiles * P.num_n_tiles * P.batch > LIM) return fail(GEMM_EPI_ERR_INVALID_VALUE, "too many tiles");
   // One row counter per 128-row block, counted in whole 256-row tiles so
   // both main-loop shapes fit.
   const size_t row_blocks = static_cast<size_t>((d.M + 2 * ge::BLOCK_M - 1) / (2 * ge::BLOCK_M)) * 2;
-  P.ws_bytes = WS_HEADER + ((row_blocks * 4 + 255) / 256) * 256;
+  P.row_blocks = static_cast<int64_t>(row_blocks);
+  P.ws_bytes = WS_HEADER + ((row_blocks * P.batch * 4 + 255) / 256) * 256;
 
   // A compiled kernel whose op list (and pair group) is exactly this one.
   P.spec = nullptr;
@@ -348,7 +377,13 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.n_al8 = static_cast<int32_t>(P.n_out / 16 * 16);
   k.num_m_tiles = static_cast<int32_t>((d.M + tile_m - 1) / tile_m);
   k.num_n_tiles = static_cast<int32_t>(P.num_n_tiles);
-  k.num_tiles = k.num_m_tiles * k.num_n_tiles;
+  k.num_tiles = k.num_m_tiles * k.num_n_tiles * static_cast<int32_t>(P.batch);
+  k.a_batched = P.batch > 1 && d.batch_stride_a != 0;
+  k.b_batched = P.batch > 1 && d.batch_stride_b != 0;
+  k.row_blocks = static_cast<int32_t>(P.row_blocks);
+  k.bs_c = P.batch > 1 ? d.batch_stride_c : 0;
+  k.bs_c8 = P.batch > 1 ? d.batch_stride_c8 : 0;
+  k.bs_aux = P.batch > 1 ? d.batch_stride_aux : 0;
   k.num_k_blocks = static_cast<int32_t>((d.K + ge::BLOCK_K - 1) / ge::BLOCK_K);
   k.group_m = DEFAULT_GROUP_M;
   k.b_kn = (d.b_layout & ~GEMM_EPI_B_DUAL) == GEMM_EPI_B_KN ? 1 : 0;
@@ -394,7 +429,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   gemm_epi_status s;
   if (d.K > 0) {
     s = make_map(&L.ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, d.K, d.M, d.lda * 2, ge::BLOCK_K, ge::BLOCK_M,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A", P.batch,
+                 k.a_batched ? d.batch_stride_a * 2 : 0);
     if (s) return s;
     // Each B operand: N (or N/2 with B2) columns; K-major boxes hold the
     // rows one CTA stages from one operand.
@@ -405,21 +441,23 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
       const void* base = which == 0 ? a.B : a.B2;
       if (k.b_kn)
         s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, b_cols, d.K, d.ldb * 2, 64, ge::BLOCK_K,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B");
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
+                     k.b_batched ? d.batch_stride_b * 2 : 0);
       else
         s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d.K, b_cols, d.ldb * 2, ge::BLOCK_K, nk_rows,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B");
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
+                     k.b_batched ? d.batch_stride_b * 2 : 0);
       if (s) return s;
     }
   }
   if ((P.flags & ge::F_STORE) && k.n_al > 0) {
     s = make_map(&L.tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, k.n_al, d.M, d.ldc * 2, ge::CHUNK, 32,
-                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
+                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C", P.batch, k.bs_c * 2);
     if (s) return s;
   }
   if ((P.flags & ge::F_E8) && k.n_al8 > 0) {
     s = make_map(&L.tc8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.C8, k.n_al8, d.M, d.ldc8, ge::CHUNK, 32,
-                 CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C8");
+                 CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C8", P.batch, k.bs_c8);
     if (s) return s;
   }
   return GEMM_EPI_OK;
@@ -461,9 +499,9 @@ gemm_epi_status clear_outputs(const gemm_epi_plan& P, const gemm_epi_args& a, cu
   cudaError_t e = cudaMemsetAsync(a.workspace, 0, P.ws_bytes, st);
   if (e == cudaSuccess && (P.flags & ge::F_AMAX)) e = cudaMemsetAsync(a.amax, 0, sizeof(float), st);
   if (e == cudaSuccess && (P.flags & ge::F_ROW) && P.d.M > 0)
-    e = cudaMemsetAsync(a.row_out, 0, sizeof(float) * P.d.M, st);
+    e = cudaMemsetAsync(a.row_out, 0, sizeof(float) * P.d.M * P.batch, st);
   if (e == cudaSuccess && (P.flags & ge::F_COL) && P.n_out > 0)
-    e = cudaMemsetAsync(a.col_out, 0, sizeof(float) * P.n_out, st);
+    e = cudaMemsetAsync(a.col_out, 0, sizeof(float) * P.n_out * P.batch, st);
   return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "cudaMemsetAsync");
 }
 
@@ -545,7 +583,8 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   g_last_error.clear();
   if (!h || !args) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and args must not be NULL");
   if (h->pair_at >= 0 && h->pair_g > 8)
-    return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass handles PAIR_SWIGLU groups up to 8");
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass handles pair groups up to 8");
+  if (h->batch > 1) return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass runs single problems");
   DeviceState* dev = nullptr;
   gemm_epi_status s = device_state(&dev, nullptr);
   if (s) return s;

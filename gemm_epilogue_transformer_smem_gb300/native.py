@@ -67,6 +67,10 @@ class gemm_epi_desc(ctypes.Structure):
         ("ldc", ctypes.c_int64), ("ldc8", ctypes.c_int64), ("ld_aux", ctypes.c_int64),
         ("b_layout", ctypes.c_int32), ("n_ops", ctypes.c_int32),
         ("ops", ctypes.POINTER(gemm_epi_op)),
+        ("batch", ctypes.c_int64),
+        ("batch_stride_a", ctypes.c_int64), ("batch_stride_b", ctypes.c_int64),
+        ("batch_stride_c", ctypes.c_int64), ("batch_stride_c8", ctypes.c_int64),
+        ("batch_stride_aux", ctypes.c_int64),
     ]
 
 

@@ -153,6 +153,14 @@ typedef struct gemm_epi_desc {
     int32_t b_layout;         /* gemm_epi_b_layout */
     int32_t n_ops;            /* 0 .. GEMM_EPI_MAX_OPS */
     const gemm_epi_op *ops;   /* copied by gemm_epi_create */
+    /* Batched GEMM (the cuDNN Graph API tutorial's batched matmul epilogue):
+     * `batch` independent problems of the same shape and program; 0 or 1 is
+     * one problem.  Strides between batches are in elements (bytes for C8);
+     * 0 for A or B (and B2) shares that operand across the batch.  Per batch:
+     * row_scale, row_out (M values each) and col_out (N_out each) advance by
+     * M and N_out; bias is shared; AMAX is one value over the whole batch. */
+    int64_t batch;
+    int64_t batch_stride_a, batch_stride_b, batch_stride_c, batch_stride_c8, batch_stride_aux;
 } gemm_epi_desc;
 
 typedef struct gemm_epi_args {

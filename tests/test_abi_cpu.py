@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_struct_layouts_match_header(lib):
     assert ctypes.sizeof(N.gemm_epi_op) == 12
-    assert ctypes.sizeof(N.gemm_epi_desc) == 8 * 8 + 4 + 4 + 8
+    assert ctypes.sizeof(N.gemm_epi_desc) == 8 * 8 + 4 + 4 + 8 + 6 * 8
     assert ctypes.sizeof(N.gemm_epi_args) == 2 * 8 + 2 * 4 + 10 * 8 + 8 + 2 * 4 + 8
 
 
@@ -172,3 +172,31 @@ def test_create_accepts_two_weight_programs(lib, layout):
         pair = any(p.startswith("pair") for p in prog)
         assert lib.gemm_epi_out_cols(h) == (256 if pair else 512)
         lib.gemm_epi_destroy(h)
+
+
+def test_create_checks_batch_strides(lib):
+    def desc(**kw):
+        ops = api.encode_program(["residual", "store_bf16", "row_rms"])
+        d = N.gemm_epi_desc(M=256, N=512, K=128, lda=128, ldb=512, ldc=512, ldc8=512, ld_aux=512,
+                            b_layout=N.GEMM_EPI_B_KN, n_ops=3, ops=ctypes.cast(ops, ctypes.POINTER(N.gemm_epi_op)))
+        d.batch, d.batch_stride_a, d.batch_stride_b = 4, 256 * 128, 128 * 512
+        d.batch_stride_c, d.batch_stride_aux = 256 * 512, 256 * 512
+        for k, v in kw.items():
+            setattr(d, k, v)
+        h = N.gemm_epi_handle()
+        return lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)), h, ops
+    s, h, _ = desc()
+    assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
+    one, h1, _ = desc(batch=1)
+    # one row counter per 128-row block of every batch
+    assert lib.gemm_epi_workspace_size(h) >= 256 + 4 * 2 * 4
+    assert lib.gemm_epi_workspace_size(h) >= lib.gemm_epi_workspace_size(h1)
+    lib.gemm_epi_destroy(h)
+    lib.gemm_epi_destroy(h1)
+    s, h, _ = desc(batch_stride_b=0)          # shared weights
+    assert s == N.GEMM_EPI_OK
+    lib.gemm_epi_destroy(h)
+    for bad in (dict(batch_stride_c=0), dict(batch_stride_c=512), dict(batch_stride_a=100),
+                dict(batch_stride_aux=256 * 512 - 8), dict(batch=-1), dict(batch=70000)):
+        s, h, _ = desc(**bad)
+        assert s == N.GEMM_EPI_ERR_INVALID_VALUE, bad
