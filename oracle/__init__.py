@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the
 cpu_baseline / reference legs of ``bench.py`` import this package.  The CUDA
 library and its Python binding never import it, and it imports nothing from
-them: inputs arrive as numpy arrays of bf16 bit patterns (uint16) and fp32.
+them: inputs arrive as numpy arrays of bf16 bit patterns (uint16), FP8
+codes (uint8) and fp32.
 
 The program is a list of op names, optionally with one numeric argument:
 ``alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
@@ -36,7 +37,13 @@ class _Problem(ctypes.Structure):
         ("ld_aux", ctypes.c_int64),
         ("fp8_scale", ctypes.c_double),
         ("program", ctypes.c_char_p),
+        ("a_type", ctypes.c_int), ("b_type", ctypes.c_int),
+        ("a_scale_inv", ctypes.c_double), ("b_scale_inv", ctypes.c_double),
     ]
+
+
+# Operand element types: bf16 bit patterns (uint16) or FP8 codes (uint8).
+TYPES = {"bf16": 0, "e4m3": 1, "e5m2": 2}
 
 
 def load():
@@ -63,6 +70,8 @@ def load():
         lib.oracle_double_to_e4m3.restype = ctypes.c_uint8
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e5m2_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e5m2_to_double.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -73,6 +82,19 @@ def _u16(a):
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
         raise TypeError("bf16 operands are passed as uint16 bit patterns")
+    return a
+
+
+def _operand(a, type_name):
+    if a is None:
+        return None
+    if type_name == "bf16":
+        return _u16(a)
+    if type_name not in TYPES:
+        raise ValueError("unknown operand type %r" % type_name)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("FP8 operands are passed as uint8 codes")
     return a
 
 
@@ -90,10 +112,13 @@ def _ptr(a):
 class Problem:
     """One GEMM + epilogue problem in the oracle's terms.
 
-    A: M x K bf16 bits (uint16), row-major with row stride ``A.shape[1]``.
-    B: K x N bf16 bits when ``b_is_nk`` is False, else N x K.
+    A: M x K bf16 bits (uint16) or FP8 codes (uint8, ``a_type`` "e4m3" or
+    "e5m2"), row-major with row stride ``A.shape[1]``.
+    B: K x N when ``b_is_nk`` is False, else N x K, of type ``b_type``.
     B2: optional second weight operand of B's shape; the accumulator then
     has 2 x B's columns, alternating between B and B2 in blocks of 128.
+    a_scale_inv, b_scale_inv: per-tensor dequantisation factors; the
+    accumulator is their product times A @ B.
     """
     A: np.ndarray
     B: np.ndarray
@@ -106,13 +131,17 @@ class Problem:
     preact: Optional[np.ndarray] = None
     fp8_scale: float = 1.0
     B2: Optional[np.ndarray] = None
+    a_type: str = "bf16"
+    b_type: str = "bf16"
+    a_scale_inv: float = 1.0
+    b_scale_inv: float = 1.0
 
     def _c(self):
-        A = _u16(self.A)
-        B = _u16(self.B)
+        A = _operand(self.A, self.a_type)
+        B = _operand(self.B, self.b_type)
         M, K = A.shape
         N = B.shape[0] if self.b_is_nk else B.shape[1]
-        B2 = _u16(self.B2)
+        B2 = _operand(self.B2, self.b_type)
         if B2 is not None:
             if B2.shape != B.shape:
                 raise ValueError("B2 must have B's shape")
@@ -132,7 +161,8 @@ class Problem:
         p = _Problem(M, N, K, 1 if self.b_is_nk else 0,
                      A.ctypes.data, A.shape[1], B.ctypes.data, B.shape[1], _ptr(B2),
                      float(self.alpha), _ptr(bias), _ptr(rs), _ptr(res), _ptr(pre),
-                     ld_aux, float(self.fp8_scale), prog)
+                     ld_aux, float(self.fp8_scale), prog, TYPES[self.a_type], TYPES[self.b_type],
+                     float(self.a_scale_inv), float(self.b_scale_inv))
         return p, keep
 
     @property
@@ -214,6 +244,12 @@ def to_e4m3(x) -> np.ndarray:
 
 def e4m3_to_f64(c) -> np.ndarray:
     f = load().oracle_e4m3_to_double
+    a = np.asarray(c, dtype=np.uint8)
+    return np.array([f(int(v)) for v in a.ravel()], dtype=np.float64).reshape(a.shape)
+
+
+def e5m2_to_f64(c) -> np.ndarray:
+    f = load().oracle_e5m2_to_double
     a = np.asarray(c, dtype=np.uint8)
     return np.array([f(int(v)) for v in a.ravel()], dtype=np.float64).reshape(a.shape)
 

@@ -8,8 +8,11 @@
  *
  * What it computes (one definition, no blocking, no fusion, no reordering):
  *
- *   acc[m,n] = sum_k A[m,k] * B[k,n]                    (fp64, exact widening
- *                                                         of the bf16 inputs)
+ *   acc[m,n] = sa * sb * sum_k A[m,k] * B[k,n]          (fp64, exact widening
+ *                                                         of the bf16 / fp8
+ *                                                         inputs; sa, sb the
+ *                                                         operands' dequant
+ *                                                         factors, 1 for bf16)
  *   then the epilogue program, op by op, in the order given, per element.
  *
  * Sources, cited by page title and section:
@@ -39,6 +42,12 @@
  *    is even/odd.
  *  - e4m3 is OCP FP8 E4M3FN (bias 7, max 448, no infinities); quantisation is
  *    round-to-nearest-even of value*scale, saturated to +-448, NaN kept.
+ *  - FP8 operands (the FP8 training loop of the cuDNN Graph API tutorial's
+ *    matmul epilogue paragraph: an AMAX-derived scale quantises the next
+ *    GEMM's input): e4m3 or e5m2 codes (OCP E5M2: bias 15, infinities and
+ *    NaNs at exponent 31) widened exactly; each operand's per-tensor
+ *    dequantisation factor (the reciprocal of its quantisation scale)
+ *    multiplies the accumulator.
  *  - row_rms averages the squares of the bf16-rounded values (what the next
  *    RMSNorm reads); row_rms_unrounded squares the fp64 values.  col_sum and
  *    amax observe the unrounded value.
@@ -135,6 +144,24 @@ double oracle_e4m3_to_double(uint8_t c)
     return s ? -v : v;
 }
 
+/* e5m2 (OCP E5M2): 1 sign, 5 exponent (bias 15), 2 fraction bits.  Normal
+ * values (1 + f/4) 2^(e-15) for e = 1..30; exponent 31 is infinity (f = 0)
+ * or NaN; subnormals f/4 * 2^-14.  Largest finite 57344. */
+double oracle_e5m2_to_double(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 2) & 0x1F, f = c & 3;
+    double v;
+    if (e == 31) {
+        if (f) return NAN;
+        v = INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)f / 4.0, -14);
+    } else {
+        v = ldexp(1.0 + (double)f / 4.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
 /* ------------------------------------------------------------------ */
 /* activations (fp64)                                                  */
 /* ------------------------------------------------------------------ */
@@ -222,9 +249,19 @@ static int parse_program(const char *s, oop *ops, int *n_out)
 /* the GEMM                                                            */
 /* ------------------------------------------------------------------ */
 
+/* Element i of an operand of the given type, widened exactly. */
+static double elem_at(const void *base, int type, int64_t i)
+{
+    switch (type) {
+    case ORACLE_E4M3: return oracle_e4m3_to_double(((const uint8_t *)base)[i]);
+    case ORACLE_E5M2: return oracle_e5m2_to_double(((const uint8_t *)base)[i]);
+    default: return oracle_bf16_to_double(((const uint16_t *)base)[i]);
+    }
+}
+
 static double a_at(const oracle_problem *p, int64_t m, int64_t k)
 {
-    return oracle_bf16_to_double(p->A[m * p->lda + k]);
+    return elem_at(p->A, p->a_type, m * p->lda + k);
 }
 
 /* Accumulator column n.  With a second weight operand B2 the columns
@@ -232,13 +269,13 @@ static double a_at(const oracle_problem *p, int64_t m, int64_t k)
  * block 2i+1 is B2's same columns. */
 static double b_at(const oracle_problem *p, int64_t k, int64_t n)
 {
-    const uint16_t *src = p->B;
+    const void *src = p->B;
     if (p->B2) {
         if ((n / 128) % 2) src = p->B2;
         n = (n / 256) * 128 + n % 128;
     }
-    return p->b_is_nk ? oracle_bf16_to_double(src[n * p->ldb + k])
-                      : oracle_bf16_to_double(src[k * p->ldb + n]);
+    return p->b_is_nk ? elem_at(src, p->b_type, n * p->ldb + k)
+                      : elem_at(src, p->b_type, k * p->ldb + n);
 }
 
 /* One whole accumulator row, i-k-j order for the K x N layout. */
@@ -248,9 +285,8 @@ static void acc_row(const oracle_problem *p, int64_t m, double *acc)
     if (!p->b_is_nk && !p->B2) {
         for (int64_t k = 0; k < p->K; ++k) {
             double a = a_at(p, m, k);
-            const uint16_t *brow = p->B + k * p->ldb;
             for (int64_t n = 0; n < p->N; ++n)
-                acc[n] += a * oracle_bf16_to_double(brow[n]);
+                acc[n] += a * elem_at(p->B, p->b_type, k * p->ldb + n);
         }
     } else {
         for (int64_t n = 0; n < p->N; ++n) {
@@ -259,6 +295,7 @@ static void acc_row(const oracle_problem *p, int64_t m, double *acc)
             acc[n] = s;
         }
     }
+    for (int64_t n = 0; n < p->N; ++n) acc[n] *= p->a_scale_inv * p->b_scale_inv;
 }
 
 /* One accumulator element. */
@@ -266,7 +303,7 @@ static double acc_elem(const oracle_problem *p, int64_t m, int64_t n)
 {
     double s = 0.0;
     for (int64_t k = 0; k < p->K; ++k) s += a_at(p, m, k) * b_at(p, k, n);
-    return s;
+    return s * p->a_scale_inv * p->b_scale_inv;
 }
 
 /* ------------------------------------------------------------------ */

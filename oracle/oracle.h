@@ -17,11 +17,11 @@ extern "C" {
 typedef struct {
     int64_t M, N, K;
     int b_is_nk;                 /* 0: B is K x N row-major; 1: B is N x K row-major */
-    const uint16_t *A;           /* bf16 bit patterns, M x K, row stride lda */
+    const void *A;               /* M x K elements of type a_type, row stride lda */
     int64_t lda;
-    const uint16_t *B;           /* bf16 bit patterns */
+    const void *B;               /* elements of type b_type */
     int64_t ldb;
-    const uint16_t *B2;          /* second weight operand or NULL (same layout, ldb) */
+    const void *B2;              /* second weight operand or NULL (same layout, ldb) */
     double alpha;                /* op "alpha" */
     const float *bias;           /* op "bias": one value per column at its point of use */
     const float *row_scale;      /* op "row_scale": M values */
@@ -30,7 +30,12 @@ typedef struct {
     int64_t ld_aux;
     double fp8_scale;            /* op "store_e4m3": code = e4m3(value * fp8_scale) */
     const char *program;         /* comma-separated op names, optional ":arg" */
+    int a_type, b_type;          /* ORACLE_BF16 (bit patterns), ORACLE_E4M3, ORACLE_E5M2 (codes) */
+    double a_scale_inv;          /* the accumulator is a_scale_inv * b_scale_inv * (A @ B) */
+    double b_scale_inv;          /* (1.0 for unscaled operands) */
 } oracle_problem;
+
+enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1, ORACLE_E5M2 = 2 };
 
 /* Whole output rows for the listed row indices (rows == NULL: rows 0..nrows-1).
  * Every output pointer may be NULL.  y: value at store_bf16 (or final value),
@@ -49,6 +54,7 @@ double oracle_bf16_to_double(uint16_t bits);
 uint16_t oracle_double_to_bf16(double x);
 uint8_t oracle_double_to_e4m3(double x);
 double oracle_e4m3_to_double(uint8_t c);
+double oracle_e5m2_to_double(uint8_t c);
 double oracle_gelu_tanh(double x);
 double oracle_gelu_tanh_grad(double x);
 double oracle_silu(double x);

@@ -394,3 +394,69 @@ def test_two_weight_pairs_match_numpy(layout, pair):
     np.testing.assert_allclose(y, f * U, rtol=1e-12, atol=1e-14)
     cols = p.cols([0, 127, 128, 383])
     np.testing.assert_allclose(cols["y"], y[:, [0, 127, 128, 383]], rtol=1e-15)
+
+
+# ---------------------------------------------------------------- FP8 operands
+
+def _torch_decode(codes, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(dtype)
+    return t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("name,dtype", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_decode_matches_torch_for_every_code(name, dtype):
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_f64(codes) if name == "e4m3" else oracle.e5m2_to_f64(codes)
+    theirs = _torch_decode(codes, dtype)
+    assert np.array_equal(np.isnan(ours), np.isnan(theirs))
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], theirs[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(theirs[ok]))
+
+
+def test_e5m2_closed_forms():
+    # 1.0, largest finite (1.75 * 2^15), smallest subnormal (2^-16), smallest
+    # normal (2^-14), -2, +inf, a NaN.
+    vals = oracle.e5m2_to_f64(np.array([0x3C, 0x7B, 0x01, 0x04, 0xC0, 0x7C, 0x7D], np.uint8))
+    assert list(vals[:6]) == [1.0, 57344.0, 2.0 ** -16, 2.0 ** -14, -2.0, math.inf]
+    assert math.isnan(vals[6])
+
+
+def _rand_fp8(shape, dtype, scale):
+    t = torch.from_numpy((RNG.standard_normal(shape) * scale).astype(np.float32)).to(dtype)
+    return t.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("a_t,b_t", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_fp8_gemm_matches_numpy_einsum(a_t, b_t, layout):
+    """Codes decoded by torch, multiplied by numpy in fp64, then scaled by
+    both dequantisation factors (distinct, so a dropped one shows)."""
+    dt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    M, N, K = 13, 21, 48
+    A = _rand_fp8((M, K), dt[a_t], 30.0)
+    B = _rand_fp8((K, N) if layout == "kn" else (N, K), dt[b_t], 30.0)
+    sa, sb = 1.0 / 30.0, 1.0 / 112.0
+    y = Problem(A, B, ["store_bf16"], b_is_nk=(layout == "nk"), a_type=a_t, b_type=b_t,
+                a_scale_inv=sa, b_scale_inv=sb).rows()["y"]
+    Ad = _torch_decode(A, dt[a_t])
+    Bd = _torch_decode(B, dt[b_t])
+    ref = np.einsum("mk,kn->mn", Ad, Bd if layout == "kn" else Bd.T) * sa * sb
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_fp8_scale_applies_before_the_program():
+    """relu(alpha * acc + bias) with the dequantisation inside acc: a bias
+    added before the scaling would give a different result."""
+    A = np.full((2, 16), 0x38, np.uint8)            # e4m3 1.0
+    B = np.full((16, 3), 0x40, np.uint8)            # e4m3 2.0
+    bias = np.array([-1.0, 0.0, 1.0], np.float32)
+    r = Problem(A, B, ["alpha", "bias", "relu", "store_bf16"], alpha=0.5, bias=bias, a_type="e4m3",
+                b_type="e4m3", a_scale_inv=0.25, b_scale_inv=0.5).rows()
+    # acc = 0.25 * 0.5 * 16 * 2 = 4; y = relu(0.5 * 4 + bias)
+    assert np.array_equal(r["y"], np.array([[1.0, 2.0, 3.0]] * 2))
+
+
+def test_fp8_operand_type_is_enforced():
+    with pytest.raises(TypeError):
+        Problem(rand_bf16((2, 16)), np.zeros((16, 2), np.uint8), [], a_type="e4m3", b_type="e4m3").rows()
