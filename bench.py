@@ -191,20 +191,35 @@ def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> fl
 
 # ------------------------------------------------------------------ oracle leg
 
+def oracle_problem(w, inp):
+    """The workload as the CPU oracle takes it: host copies of the same bf16
+    bit patterns or FP8 codes, the same scalars."""
+    import oracle
+    from gemm_epilogue_transformer_smem_gb300 import synth
+
+    def operand(t):
+        if t is None:
+            return None
+        return synth.bf16_bits(t) if w.in_type == "bf16" else t.contiguous().cpu().numpy()
+
+    def scalar(t):
+        return 1.0 if t is None else float(t.item())
+
+    aux = synth.bf16_bits(inp.aux) if inp.aux is not None else None
+    return oracle.Problem(operand(inp.A), operand(inp.B), list(w.program), b_is_nk=(w.b_layout == "nk"),
+                          alpha=inp.alpha, bias=None if inp.bias is None else inp.bias.cpu().numpy(),
+                          residual=aux if w.aux == "residual" else None,
+                          preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
+                          B2=operand(inp.B2), a_type=w.in_type, b_type=w.in_type,
+                          a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv))
+
+
 def oracle_rows_sample(w, inp, seconds: float):
     """Times the CPU oracle on leading rows of the workload, growing the row
     count until about `seconds` of work.  Returns (tflops, rows, threads)."""
     import oracle
-    from gemm_epilogue_transformer_smem_gb300 import synth
 
-    A = synth.bf16_bits(inp.A)
-    B = synth.bf16_bits(inp.B)
-    aux = synth.bf16_bits(inp.aux) if inp.aux is not None else None
-    prob = oracle.Problem(A, B, list(w.program), b_is_nk=(w.b_layout == "nk"), alpha=inp.alpha,
-                          bias=None if inp.bias is None else inp.bias.cpu().numpy(),
-                          residual=aux if w.aux == "residual" else None,
-                          preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
-                          B2=synth.bf16_bits(inp.B2) if inp.B2 is not None else None)
+    prob = oracle_problem(w, inp)
     threads = oracle.cpu_threads()
     rows = max(1, min(w.M, threads))
     while True:
@@ -233,14 +248,7 @@ def run_reference(args, world, rank):
     per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     # size one step once, then run warmup + steps of that size
     _, rows, threads, _ = oracle_rows_sample(w, inp, per_step)
-    import oracle
-    prob = oracle.Problem(synth.bf16_bits(inp.A), synth.bf16_bits(inp.B), list(w.program),
-                          b_is_nk=(w.b_layout == "nk"), alpha=inp.alpha,
-                          bias=None if inp.bias is None else inp.bias.numpy(),
-                          residual=synth.bf16_bits(inp.aux) if w.aux == "residual" else None,
-                          preact=synth.bf16_bits(inp.aux) if w.aux == "preact" else None,
-                          fp8_scale=inp.fp8_scale,
-                          B2=synth.bf16_bits(inp.B2) if inp.B2 is not None else None)
+    prob = oracle_problem(w, inp)
     for _ in range(args.warmup):
         prob.rows(list(range(rows)))
     t0 = time.perf_counter()
@@ -287,10 +295,12 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
     inp = synth.make_inputs(w, dev)
-    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual)
+    types = dict(a_type=w.in_type, b_type=w.in_type)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, **types)
     out = api.allocate_outputs(plan, dev)
     stream = torch.cuda.current_stream(dev)
-    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2)
+    scales = dict(a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv)
+    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2, **scales)
 
     def step():
         api.run_program(plan, inp.A, inp.B, out, **kw)
@@ -325,11 +335,11 @@ def run_ours(args, world, rank, local):
         # Fused, bare GEMM (same main loop, store-only program) and unfused
         # (bare GEMM + separate epilogue pass) timed in interleaved rounds so
         # that all three see the same clock and power state; medians.
-        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual)
+        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual, **types)
         bare_out = api.allocate_outputs(bare, dev)
 
         def bare_step():
-            bare.run(inp.A, inp.B, C=bare_out.C, workspace=bare_out.workspace, B2=inp.B2)
+            bare.run(inp.A, inp.B, C=bare_out.C, workspace=bare_out.workspace, B2=inp.B2, **scales)
 
         scratch = bare_out.C
 
@@ -370,10 +380,15 @@ def run_ours(args, world, rank, local):
         return
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_source = "%s burst bf16 (cuBLAS)" % src
+    if w.in_type != "bf16":
+        # FP8 operands: the measured bf16 peak times the nominal dense
+        # FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s).
+        peak *= 2.0
+        peak_source = "%s burst bf16 (cuBLAS) x 2, the nominal dense fp8/bf16 ratio" % src
     traffic = profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": fused_tflops / peak, "traffic": traffic,
-                "peak_source": "%s burst bf16 (cuBLAS)" % src,
+                "frac": fused_tflops / peak, "traffic": traffic, "peak_source": peak_source,
                 "algorithmic_flops_per_launch": flops}
     cpu = None
     if not args.no_cpu:
@@ -385,7 +400,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.in_type == "bf16" else w.in_type,
+        "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "b_layout": w.b_layout,
                    "program": list(w.program), "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: inputs + output (%d MB) exceed the 129 MB L2" % (
@@ -408,7 +424,8 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
     from gemm_epilogue_transformer_smem_gb300 import api
 
     h = {k: (v.cpu().pin_memory() if v is not None else None)
-         for k, v in (("A", inp.A), ("B", inp.B), ("bias", inp.bias), ("aux", inp.aux), ("B2", inp.B2))}
+         for k, v in (("A", inp.A), ("B", inp.B), ("bias", inp.bias), ("aux", inp.aux), ("B2", inp.B2),
+                      ("a_scale_inv", inp.a_scale_inv), ("b_scale_inv", inp.b_scale_inv))}
     d = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
     outs = [t for t in (out.C, out.C8, out.amax, out.row_out, out.col_out) if t is not None]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
@@ -421,7 +438,8 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
             if v is not None:
                 d[k].copy_(v, non_blocking=True)
         api.run_program(plan, d["A"], d["B"], out, alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
-                        bias=d["bias"], aux=d["aux"], B2=d["B2"])
+                        bias=d["bias"], aux=d["aux"], B2=d["B2"], a_scale_inv=d["a_scale_inv"],
+                        b_scale_inv=d["b_scale_inv"])
         for t, ht in zip(outs, host_out):
             ht.copy_(t, non_blocking=True)
 

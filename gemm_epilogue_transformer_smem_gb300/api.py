@@ -60,6 +60,11 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+# Operand element types (desc.a_type / b_type); 8-bit operands are passed as
+# uint8 (or torch float8) tensors of codes.
+OPERAND_TYPES = {"bf16": N.GEMM_EPI_TYPE_BF16, "e4m3": N.GEMM_EPI_TYPE_E4M3, "e5m2": N.GEMM_EPI_TYPE_E5M2}
+
+
 class Plan:
     """One validated GEMM + epilogue plan (gemm_epi_create).  Strides default
     to tight row-major packing."""
@@ -69,7 +74,8 @@ class Plan:
                  ldc8: Optional[int] = None, ld_aux: Optional[int] = None, dual: bool = False,
                  batch: int = 1, batch_stride_a: Optional[int] = None,
                  batch_stride_b: Optional[int] = None, batch_stride_c: Optional[int] = None,
-                 batch_stride_c8: Optional[int] = None, batch_stride_aux: Optional[int] = None):
+                 batch_stride_c8: Optional[int] = None, batch_stride_aux: Optional[int] = None,
+                 a_type: str = "bf16", b_type: str = "bf16"):
         self.lib = N.load()
         self.program = list(program)
         self.M, self.N, self.K = M, N_, K
@@ -98,6 +104,8 @@ class Plan:
         d.batch_stride_c8 = M * d.ldc8 if batch_stride_c8 is None else batch_stride_c8
         d.batch_stride_aux = M * d.ld_aux if batch_stride_aux is None else batch_stride_aux
         self.batch = batch
+        d.a_type, d.b_type = OPERAND_TYPES[a_type], OPERAND_TYPES[b_type]
+        self.a_type, self.b_type = a_type, b_type
         self.desc = d
         h = N.gemm_epi_handle()
         N.check(self.lib.gemm_epi_create(ctypes.byref(h), ctypes.byref(d)), self.lib)
@@ -113,9 +121,10 @@ class Plan:
 
     def args(self, A, B, *, alpha=1.0, fp8_scale=1.0, bias=None, row_scale=None, residual=None,
              preact=None, C=None, C8=None, amax=None, row_out=None, col_out=None, workspace=None,
-             timeout_ms=0, debug_flags=0, B2=None) -> N.gemm_epi_args:
+             timeout_ms=0, debug_flags=0, B2=None, a_scale_inv=None, b_scale_inv=None) -> N.gemm_epi_args:
         a = N.gemm_epi_args()
         a.A, a.B, a.B2 = _ptr(A), _ptr(B), _ptr(B2)
+        a.a_scale_inv, a.b_scale_inv = _ptr(a_scale_inv), _ptr(b_scale_inv)
         a.alpha, a.fp8_scale = float(alpha), float(fp8_scale)
         a.bias, a.row_scale = _ptr(bias), _ptr(row_scale)
         a.residual, a.preact = _ptr(residual), _ptr(preact)

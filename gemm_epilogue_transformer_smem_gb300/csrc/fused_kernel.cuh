@@ -52,8 +52,8 @@ namespace ge {
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 256;
-constexpr int BLOCK_K = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int UMMA_K = 16;
+constexpr int BLOCK_K = 64;  // 64 bf16 = 128 bytes = one swizzle row (128 FP8 elements)
+constexpr int UMMA_K = 16;   // bf16 elements per MMA = 32 bytes of a row (32 FP8 elements)
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int CHUNK = 32;     // output columns per epilogue step
@@ -100,6 +100,7 @@ enum : uint32_t {
   F_ROW = 1u << 4,
   F_COL = 1u << 5,
   F_ZERO_ACC = 1u << 6,  // K == 0: the accumulator is zero, TMEM is not read
+  F_DEQ = 1u << 7,       // the accumulator is multiplied by the operands' dequantisation factors
 };
 
 // Where a bounded wait ran out (second status word).
@@ -130,6 +131,10 @@ struct KernelParams {
   int32_t dual;  // 1: accumulator columns alternate between B and B2 in 128-column blocks
   int32_t a_batched, b_batched;  // operand advances with the batch (else shared)
   int32_t row_blocks;            // row counters per batch
+  int32_t in8;                   // 1: 8-bit operands (kind::f8f6f4), a K block holds 128 elements
+  int32_t k_step;                // elements of K per block: 64 (bf16) or 128 (8-bit)
+  const float* a_scale_inv;      // dequantisation factors (F_DEQ), NULL = 1
+  const float* b_scale_inv;
   int64_t bs_c, bs_c8, bs_aux;   // batch strides for direct accesses (elements; bytes for C8)
   uint32_t idesc;
   uint32_t flags;
@@ -567,7 +572,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
             if (CG == 1) {
               ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + L::B_STAGE_BYTES);
-              ptx::tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, a_row, za);
+              ptx::tma_load_3d(sa, &tm_a, fb, kb * p.k_step, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j) {
@@ -578,23 +583,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
               } else if (p.dual) {
                 // two 128-row K-major boxes, one per operand, stacked in the stage
-                ptx::tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, b_col, zb);
-                ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * BLOCK_K, b_col, zb);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * p.k_step, b_col, zb);
+                ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * p.k_step, b_col, zb);
               } else {
-                ptx::tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, b_col, zb);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * p.k_step, b_col, zb);
               }
             } else {
               // Both CTAs' halves complete on the even CTA's full barrier,
               // which expects the bytes of the whole pair.
               const uint32_t fb0 = ptx::mapa_shared(fb, 0);
               if (rank == 0) ptx::mbar_arrive_expect_tx(fb, 2u * (A_STAGE_BYTES + L::B_STAGE_BYTES));
-              ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * BLOCK_K, a_row, za);
+              ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * p.k_step, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j)
                   ptx::tma_load_3d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K, zb);
               } else {
-                ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * BLOCK_K, b_col, zb);
+                ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * p.k_step, b_col, zb);
               }
             }
             issued |= 1u << stage;
@@ -647,15 +652,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_after_sync();
           const uint32_t sa = sbase + L::OFF_A + stage * A_STAGE_BYTES;
           const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
+          // Each MMA consumes 32 bytes of every operand row: 16 bf16 or 32
+          // FP8 elements, so both kinds step through a stage the same way.
 #pragma unroll
           for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
             const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
             const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
                                        : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
-            if (CG == 1)
-              ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+            if (CG == 1) {
+              if (p.in8)
+                ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, acc);
+              else
+                ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, acc);
+            } else {
+              if (p.in8)
+                ptx::mma_f8_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
+              else
+                ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
+            }
           }
           any_mma = true;
           if (CG == 1)
@@ -693,7 +708,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
     const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
     // A static program fixes every flag but the K == 0 one at compile time.
-    const uint32_t flags = kStatic ? (p.flags & F_ZERO_ACC) | static_flags<Prog>() : p.flags;
+    const uint32_t flags = kStatic ? (p.flags & (F_ZERO_ACC | F_DEQ)) | static_flags<Prog>() : p.flags;
+    // Product of the dequantisation factors, in fp32 (1 without F_DEQ).
+    const float deq = (flags & F_DEQ) ? (p.a_scale_inv ? __ldg(p.a_scale_inv) : 1.0f) *
+                                            (p.b_scale_inv ? __ldg(p.b_scale_inv) : 1.0f)
+                                      : 1.0f;
     const uint32_t epi0 = sbase + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
     const uint32_t e80 = sbase + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     uint8_t* epi0_ptr = smem + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
@@ -756,6 +775,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_ld32_sync(t_row + c * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            if (flags & F_DEQ) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] *= deq;
+            }
           }
         } else {
           float a[64];
@@ -772,6 +795,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tmem_ld64_sync(t_row + c * 64, t_row + c * 64 + 32, r);
 #pragma unroll
             for (int j = 0; j < 64; ++j) a[j] = __uint_as_float(r[j]);
+            if (flags & F_DEQ) {
+#pragma unroll
+              for (int j = 0; j < 64; ++j) a[j] *= deq;
+            }
           }
           if constexpr (kStatic) {
             static_for<0, (prog_pair_at<Prog>() < 0 ? 0 : prog_pair_at<Prog>())>([&](auto I) {

@@ -177,6 +177,7 @@ struct gemm_epi_plan {
   int64_t n_out = 0;
   int pair_at = -1, pair_g = 1, pair_silu = 1;
   bool dual = false;  // GEMM_EPI_B_DUAL: B columns alternate with B2 in 128-column blocks
+  bool in8 = false;   // 8-bit operands (kind::f8f6f4)
   int64_t batch = 1, row_blocks = 0;
   uint32_t flags = 0;
   bool uses_bias = false, uses_row_scale = false, uses_residual = false, uses_preact = false;
@@ -201,6 +202,14 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   if (P.dual && d.N % 256 != 0)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "GEMM_EPI_B_DUAL needs N %% 256 == 0 (N=%lld)",
                 static_cast<long long>(d.N));
+  if (d.a_type < GEMM_EPI_TYPE_BF16 || d.a_type > GEMM_EPI_TYPE_E5M2 || d.b_type < GEMM_EPI_TYPE_BF16 ||
+      d.b_type > GEMM_EPI_TYPE_E5M2)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "unknown operand type (a_type %d, b_type %d)", d.a_type, d.b_type);
+  P.in8 = d.a_type != GEMM_EPI_TYPE_BF16;
+  if (P.in8 != (d.b_type != GEMM_EPI_TYPE_BF16))
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "A and B must both be BF16 or both 8-bit");
+  if (P.in8 && b_base != GEMM_EPI_B_NK)
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "8-bit operands need B stored N x K (GEMM_EPI_B_NK)");
   if (d.n_ops < 0 || d.n_ops > GEMM_EPI_MAX_OPS)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "n_ops must be in [0, %d]", GEMM_EPI_MAX_OPS);
   if (d.n_ops > 0 && !d.ops) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ops is NULL");
@@ -270,12 +279,16 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   // Strides: bounds first, then the 16-byte TMA rule.
   const bool kn = b_base == GEMM_EPI_B_KN;
   const int64_t b_cols = P.dual ? d.N / 2 : d.N;  // columns of each B operand
-  if (d.K % 8)  // the K tail of a TMA box is clipped in 16-byte groups
-    return fail(GEMM_EPI_ERR_MISALIGNED, "K must be a multiple of 8 (got %lld)", static_cast<long long>(d.K));
+  // Operand elements per 16-byte group: 8 bf16 or 16 FP8.
+  const int64_t op_group = P.in8 ? 16 : 8;
+  if (d.K % op_group)  // the K tail of a TMA box is clipped in 16-byte groups
+    return fail(GEMM_EPI_ERR_MISALIGNED, "K must be a multiple of %lld (got %lld)",
+                static_cast<long long>(op_group), static_cast<long long>(d.K));
   if (d.K > 0) {  // A and B are not read when K == 0
     if (d.lda < d.K) return fail(GEMM_EPI_ERR_INVALID_VALUE, "lda < K");
     if (d.ldb < (kn ? b_cols : d.K) || d.ldb <= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldb too small");
-    if (d.lda % 8 || d.ldb % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "lda and ldb must be multiples of 8");
+    if (d.lda % op_group || d.ldb % op_group)
+      return fail(GEMM_EPI_ERR_MISALIGNED, "lda and ldb must be multiples of %lld", static_cast<long long>(op_group));
   }
   if ((P.flags & ge::F_STORE) && (d.ldc < P.n_out || d.ldc <= 0))
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "ldc < output columns");
@@ -301,10 +314,10 @@ gemm_epi_status validate(gemm_epi_plan& P) {
       if (st == 0) return !may_share;
       return st < need || st % mult != 0;
     };
-    if (d.K > 0 && (bad_stride(d.batch_stride_a, d.M * d.lda, 8, true) ||
-                    bad_stride(d.batch_stride_b, b_rows * d.ldb, 8, true)))
+    if (d.K > 0 && (bad_stride(d.batch_stride_a, d.M * d.lda, op_group, true) ||
+                    bad_stride(d.batch_stride_b, b_rows * d.ldb, op_group, true)))
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "A / B batch strides must be 0 (shared) or span a whole "
-                                              "operand, in multiples of 8 elements");
+                                              "operand, in multiples of 16 bytes");
     if ((P.flags & ge::F_STORE) && bad_stride(d.batch_stride_c, d.M * d.ldc, 8, false))
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "batch_stride_c must span M x ldc, a multiple of 8");
     if ((P.flags & ge::F_E8) && bad_stride(d.batch_stride_c8, d.M * d.ldc8, 16, false))
@@ -384,15 +397,25 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.bs_c = P.batch > 1 ? d.batch_stride_c : 0;
   k.bs_c8 = P.batch > 1 ? d.batch_stride_c8 : 0;
   k.bs_aux = P.batch > 1 ? d.batch_stride_aux : 0;
-  k.num_k_blocks = static_cast<int32_t>((d.K + ge::BLOCK_K - 1) / ge::BLOCK_K);
+  // A K block is one 128-byte swizzle row of each operand: 64 bf16 or 128
+  // 8-bit elements.
+  k.in8 = P.in8 ? 1 : 0;
+  k.k_step = P.in8 ? 2 * ge::BLOCK_K : ge::BLOCK_K;
+  k.num_k_blocks = static_cast<int32_t>((d.K + k.k_step - 1) / k.k_step);
   k.group_m = DEFAULT_GROUP_M;
   k.b_kn = (d.b_layout & ~GEMM_EPI_B_DUAL) == GEMM_EPI_B_KN ? 1 : 0;
   k.dual = P.dual ? 1 : 0;
-  // Instruction descriptor: D fp32, A and B bf16, A K-major, B K- or
-  // MN-major, N = 256, M = 128 per CTA of the group.
-  k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (k.b_kn ? (1u << 16) : 0u) |
+  // Instruction descriptor: D fp32 (bits 4-5), A and B formats (bits 7-9,
+  // 10-12: bf16 = 1 for kind::f16; e4m3 = 0, e5m2 = 1 for kind::f8f6f4),
+  // A K-major, B K- or MN-major (bit 16), N >> 3 (bits 17-22), M >> 4
+  // (bits 24-28) with M = 128 per CTA of the group.
+  auto fmt = [](int32_t t) -> uint32_t { return t == GEMM_EPI_TYPE_E4M3 ? 0u : 1u; };  // bf16 or e5m2: 1
+  k.idesc = (1u << 4) | (fmt(d.a_type) << 7) | (fmt(d.b_type) << 10) | (k.b_kn ? (1u << 16) : 0u) |
             (static_cast<uint32_t>(ge::BLOCK_N >> 3) << 17) | (static_cast<uint32_t>(tile_m >> 4) << 24);
   k.flags = P.flags;
+  if (a.a_scale_inv || a.b_scale_inv) k.flags |= ge::F_DEQ;
+  k.a_scale_inv = a.a_scale_inv;
+  k.b_scale_inv = a.b_scale_inv;
   k.n_ops = static_cast<int32_t>(P.ops.size());
   k.pair_at = P.pair_at;
   k.pair_g = P.pair_g;
@@ -428,9 +451,10 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
 
   gemm_epi_status s;
   if (d.K > 0) {
-    s = make_map(&L.ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, d.K, d.M, d.lda * 2, ge::BLOCK_K, ge::BLOCK_M,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A", P.batch,
-                 k.a_batched ? d.batch_stride_a * 2 : 0);
+    const CUtensorMapDataType op_dt = P.in8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int64_t esz = P.in8 ? 1 : 2;  // bytes per operand element
+    s = make_map(&L.ta, op_dt, a.A, d.K, d.M, d.lda * esz, k.k_step, ge::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A", P.batch, k.a_batched ? d.batch_stride_a * esz : 0);
     if (s) return s;
     // Each B operand: N (or N/2 with B2) columns; K-major boxes hold the
     // rows one CTA stages from one operand.
@@ -444,9 +468,9 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
                      k.b_batched ? d.batch_stride_b * 2 : 0);
       else
-        s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d.K, b_cols, d.ldb * 2, ge::BLOCK_K, nk_rows,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
-                     k.b_batched ? d.batch_stride_b * 2 : 0);
+        s = make_map(map, op_dt, base, d.K, b_cols, d.ldb * esz, k.k_step, nk_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
+                     k.b_batched ? d.batch_stride_b * esz : 0);
       if (s) return s;
     }
   }
@@ -485,6 +509,9 @@ gemm_epi_status check_args(const gemm_epi_plan& P, const gemm_epi_args& a) {
     if (P.uses_preact && (s = need(a.preact, "preact"))) return s;
   }
   if ((P.flags & ge::F_AMAX) && (s = need(a.amax, "amax"))) return s;
+  for (const float* sc : {a.a_scale_inv, a.b_scale_inv})
+    if (sc && (reinterpret_cast<uintptr_t>(sc) & 3u))
+      return fail(GEMM_EPI_ERR_MISALIGNED, "a_scale_inv / b_scale_inv must be 4-byte aligned");
   if ((P.flags & ge::F_ROW) && d.M > 0 && (s = need(a.row_out, "row_out"))) return s;
   if ((P.flags & ge::F_COL) && P.n_out > 0 && (s = need(a.col_out, "col_out"))) return s;
   if (!a.workspace || !aligned16(a.workspace) || a.workspace_bytes < P.ws_bytes)

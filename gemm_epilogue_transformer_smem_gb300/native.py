@@ -26,6 +26,11 @@ STATUS_NAMES = {
     6: "GEMM_EPI_ERR_TIMEOUT", 7: "GEMM_EPI_ERR_WORKSPACE",
 }
 
+# gemm_epi_type
+GEMM_EPI_TYPE_BF16 = 0
+GEMM_EPI_TYPE_E4M3 = 1
+GEMM_EPI_TYPE_E5M2 = 2
+
 # gemm_epi_b_layout
 GEMM_EPI_B_KN = 0
 GEMM_EPI_B_NK = 1
@@ -71,6 +76,7 @@ class gemm_epi_desc(ctypes.Structure):
         ("batch_stride_a", ctypes.c_int64), ("batch_stride_b", ctypes.c_int64),
         ("batch_stride_c", ctypes.c_int64), ("batch_stride_c8", ctypes.c_int64),
         ("batch_stride_aux", ctypes.c_int64),
+        ("a_type", ctypes.c_int32), ("b_type", ctypes.c_int32),
     ]
 
 
@@ -85,6 +91,7 @@ class gemm_epi_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("timeout_ms", ctypes.c_uint32), ("debug_flags", ctypes.c_uint32),
         ("B2", ctypes.c_void_p),
+        ("a_scale_inv", ctypes.c_void_p), ("b_scale_inv", ctypes.c_void_p),
     ]
 
 

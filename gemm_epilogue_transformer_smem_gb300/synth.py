@@ -22,10 +22,20 @@ them; "N(0, s)" has standard deviation s):
   backward  dX = (dY @ W^T) * gelu_tanh'(preact), column sums of dX.
             dY 8192x4096 N(0,1); W 16384x4096 N(0, 0.02); preact 8192x16384
             N(0,1).
+  fp8in     the fp8 workload's program on FP8 operands: the next layer of the
+            FP8 loop reads the e4m3 activations the fp8 workload emits.
+            M = N = K = 8192.  A: e4m3 codes of max(N(0, 0.1), 0) * 112 (the
+            fp8 workload's output distribution, its bias dominating, at its
+            scale 448/4), dequantised by 1/112.  B: a weight stored N x K,
+            N(0,1)/sqrt(K), as e4m3 codes at scale 112 * sqrt(K) (448/4 of its
+            own standard deviation), dequantised by the reciprocal.
 
 Draw order per workload: A, B, bias, residual / preact, B2.  Each tensor is drawn
 in fp32 with ``torch.randn`` from one generator seeded with 1000 + index,
-scaled, then cast to bf16 (round to nearest even); bias stays fp32.
+scaled, then cast to bf16 (round to nearest even); bias stays fp32.  FP8
+operands are multiplied by their quantisation scale, clamped to the format's
+largest finite value and cast with torch (round to nearest even); the
+reciprocal scales travel as one-element fp32 device tensors.
 """
 from __future__ import annotations
 
@@ -53,6 +63,10 @@ class Workload:
     alpha: float = 1.0
     fp8_scale: float = 1.0
     dual: bool = False   # B holds gate columns, B2 the matching up columns (N/2 each)
+    in_type: str = "bf16"   # operand type of A and B: "bf16" or "e4m3"
+    a_relu: bool = False    # A drawn as max(N(0, a_std), 0)
+    a_qscale: float = 1.0   # FP8 quantisation scales of A and B
+    b_qscale: float = 1.0
     notes: str = ""
 
     @property
@@ -69,10 +83,11 @@ class Workload:
         a_std, b_std = self.a_std, self.b_std
         if self.name in ("tiny", "fp8", "downproj"):
             a_std = 1.0 / math.sqrt(K)
-        if self.name in ("tiny", "fp8"):
+        if self.name in ("tiny", "fp8", "fp8in"):
             b_std = 1.0 / math.sqrt(K)
+        b_qscale = 112.0 * math.sqrt(K) if self.name == "fp8in" else self.b_qscale
         return replace(self, name=name or "%s_%dx%dx%d" % (self.name, M, N, K), M=M, N=N, K=K,
-                       a_std=a_std, b_std=b_std)
+                       a_std=a_std, b_std=b_std, b_qscale=b_qscale)
 
 
 WORKLOADS = {
@@ -96,6 +111,11 @@ WORKLOADS = {
     "backward": Workload("backward", 4, 8192, 16384, 4096, "nk",
                          ("gelu_tanh_grad", "store_bf16", "col_sum"),
                          a_std=1.0, b_std=0.02, aux="preact"),
+    "fp8in": Workload("fp8in", 6, 8192, 8192, 8192, "nk",
+                      ("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"),
+                      a_std=0.1, b_std=1 / math.sqrt(8192), bias_std=0.1, alpha=0.5,
+                      fp8_scale=448.0 / 4.0, in_type="e4m3", a_relu=True, a_qscale=112.0,
+                      b_qscale=112.0 * math.sqrt(8192)),
 }
 
 BY_INDEX = {w.index: w for w in WORKLOADS.values()}
@@ -110,6 +130,8 @@ class Inputs:
     alpha: float
     fp8_scale: float
     B2: Optional[torch.Tensor] = None  # second weight operand, B's shape
+    a_scale_inv: Optional[torch.Tensor] = None  # FP8 dequantisation factors, 1 fp32 each
+    b_scale_inv: Optional[torch.Tensor] = None
     extra: dict = field(default_factory=dict)
 
 
@@ -132,14 +154,32 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs
         t.mul_(std)
         return t.to(dtype)
 
-    A = draw((w.M, w.K), w.a_std)
+    def operand(shape, std, qscale, relu=False):
+        if w.in_type == "bf16":
+            t = draw(shape, std, torch.float32)
+            return (t.clamp_min_(0) if relu else t).to(torch.bfloat16)
+        t = draw(shape, std, torch.float32)
+        if relu:
+            t.clamp_min_(0)
+        fmt = FP8_FORMATS[w.in_type]
+        lim = torch.finfo(fmt).max
+        return (t * qscale).clamp_(-lim, lim).to(fmt).view(torch.uint8)
+
+    A = operand((w.M, w.K), w.a_std, w.a_qscale, w.a_relu)
     nbc = w.N // 2 if w.dual else w.N
-    B = draw((w.K, nbc) if w.b_layout == "kn" else (nbc, w.K), w.b_std)
+    B = operand((w.K, nbc) if w.b_layout == "kn" else (nbc, w.K), w.b_std, w.b_qscale)
     nb = _bias_len(w)
     bias = draw((nb,), w.bias_std, torch.float32) if nb else None
     aux = draw((w.M, w.n_out), w.aux_std) if w.aux else None
-    B2 = draw(tuple(B.shape), w.b_std) if w.dual else None
-    return Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale, B2=B2)
+    B2 = operand(tuple(B.shape), w.b_std, w.b_qscale) if w.dual else None
+    inp = Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale, B2=B2)
+    if w.in_type != "bf16":
+        inp.a_scale_inv = torch.tensor([1.0 / w.a_qscale], dtype=torch.float32, device=device)
+        inp.b_scale_inv = torch.tensor([1.0 / w.b_qscale], dtype=torch.float32, device=device)
+    return inp
+
+
+FP8_FORMATS = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 def bf16_bits(t: torch.Tensor):

@@ -1,8 +1,9 @@
 /*
  * gemm_epi.h -- C ABI of the GB300 (sm_103a) fused GEMM + epilogue engine.
  *
- * One call computes   acc = A @ B   (bf16 x bf16 -> fp32 accumulate, on the
- * tcgen05 tensor cores) and, while each output tile is still on chip, runs a
+ * One call computes   acc = A @ B   (bf16 x bf16, or FP8 x FP8 with per-tensor
+ * dequantisation factors, -> fp32 accumulate, on the tcgen05 tensor cores)
+ * and, while each output tile is still on chip, runs a
  * short epilogue program on it: scaling, bias, row scale, residual add,
  * activations, a pairwise SwiGLU on interleaved gate/up columns, the GELU-tanh
  * derivative, AMAX, row RMS statistics, column sums, and bf16 / FP8-e4m3
@@ -18,7 +19,10 @@
  *    final store: the TileLang tutorial, fused GEMM epilogue paragraph.
  *  - alpha given as a host scalar, bias, activation and an AMAX reduction in
  *    the same kernel for the next FP8 quantisation: "Huong dan su dung NVIDIA
- *    cuDNN Graph API" (aihot.vn), batched matmul epilogue paragraph.
+ *    cuDNN Graph API" (aihot.vn), batched matmul epilogue paragraph.  The
+ *    next GEMM of that FP8 loop reads the e4m3 output as an FP8 operand and
+ *    multiplies the accumulator by the reciprocal of its scale (a_type,
+ *    b_type, a_scale_inv, b_scale_inv).
  *  - SwiGLU out = up * silu(gate): Superoptimizer, section 7 "SwiGLU"; the
  *    RMSNorm-MLP's out = up * gate on rows scaled by S: section 10.
  *  - RMSNorm S = 1/sqrt(mean(x^2) + eps) and the row-broadcast rewrite
@@ -43,11 +47,15 @@
  *    never accumulated across calls.
  *
  * Layouts (all row-major, strides in elements unless stated)
- *  - A: M x K bf16, row stride lda >= K.
- *  - B: GEMM_EPI_B_KN: K x N bf16, row stride ldb >= N;
- *       GEMM_EPI_B_NK: N x K bf16 (B = W^T for a weight W stored N x K),
+ *  - A: M x K of desc.a_type (bf16 by default), row stride lda >= K.
+ *  - B: GEMM_EPI_B_KN: K x N of desc.b_type, row stride ldb >= N;
+ *       GEMM_EPI_B_NK: N x K (B = W^T for a weight W stored N x K),
  *       row stride ldb >= K.  With GEMM_EPI_B_DUAL, B and B2 each hold N/2
  *       columns (K x N/2, or N/2 x K), both with row stride ldb.
+ *  - FP8 operands (a_type and b_type both E4M3 or E5M2, in any mix) are one
+ *    byte per element, so lda, ldb and their batch strides count bytes; B
+ *    must be GEMM_EPI_B_NK (K contiguous, the usual N x K weight) and K a
+ *    multiple of 16.
  *  - Output columns: N_out = N, or N/2 after GEMM_EPI_OP_PAIR_SWIGLU.
  *  - C: M x N_out bf16, row stride ldc >= N_out.  C8: M x N_out e4m3 bytes,
  *    row stride ldc8 >= N_out (bytes).
@@ -94,6 +102,14 @@ typedef enum gemm_epi_status {
     GEMM_EPI_ERR_TIMEOUT = 6,       /* a bounded in-kernel wait ran out */
     GEMM_EPI_ERR_WORKSPACE = 7      /* workspace missing or smaller than required */
 } gemm_epi_status;
+
+/* Element types of the GEMM operands.  A and B are both BF16, or both 8-bit
+ * (E4M3 and E5M2 may be mixed). */
+typedef enum gemm_epi_type {
+    GEMM_EPI_TYPE_BF16 = 0,
+    GEMM_EPI_TYPE_E4M3 = 1,   /* OCP FP8 E4M3FN */
+    GEMM_EPI_TYPE_E5M2 = 2    /* OCP FP8 E5M2 */
+} gemm_epi_type;
 
 typedef enum gemm_epi_b_layout {
     GEMM_EPI_B_KN = 0,   /* B stored K x N row-major (N contiguous) */
@@ -145,8 +161,9 @@ typedef struct gemm_epi_op {
 #define GEMM_EPI_MAX_OPS 16
 
 typedef struct gemm_epi_desc {
-    int64_t M, N, K;          /* GEMM sizes; M, N >= 0; K >= 0, K % 8 == 0 (K == 0: acc = 0) */
-    int64_t lda, ldb;         /* row strides of A and B, elements */
+    int64_t M, N, K;          /* GEMM sizes; M, N >= 0; K >= 0, K % 8 == 0 (K % 16 == 0 for FP8
+                                 operands; K == 0: acc = 0) */
+    int64_t lda, ldb;         /* row strides of A and B, elements (bytes for FP8) */
     int64_t ldc;              /* row stride of C (bf16 elements); used with STORE_BF16 */
     int64_t ldc8;             /* row stride of C8 (bytes); used with STORE_E4M3 */
     int64_t ld_aux;           /* row stride of residual / preact (elements) */
@@ -161,11 +178,12 @@ typedef struct gemm_epi_desc {
      * M and N_out; bias is shared; AMAX is one value over the whole batch. */
     int64_t batch;
     int64_t batch_stride_a, batch_stride_b, batch_stride_c, batch_stride_c8, batch_stride_aux;
+    int32_t a_type, b_type;   /* gemm_epi_type of A and of B (and B2); 0 = BF16 */
 } gemm_epi_desc;
 
 typedef struct gemm_epi_args {
-    const void *A;            /* bf16, device */
-    const void *B;            /* bf16, device */
+    const void *A;            /* desc.a_type, device */
+    const void *B;            /* desc.b_type, device */
     float alpha;              /* SCALE_ALPHA */
     float fp8_scale;          /* STORE_E4M3 */
     const float *bias;        /* ADD_BIAS_COL */
@@ -181,7 +199,15 @@ typedef struct gemm_epi_args {
     size_t workspace_bytes;
     uint32_t timeout_ms;      /* bound of every in-kernel wait; 0 = 2000 ms */
     uint32_t debug_flags;     /* 0 in normal use; GEMM_EPI_DEBUG_* for tests */
-    const void *B2;           /* second weight operand with GEMM_EPI_B_DUAL, bf16 */
+    const void *B2;           /* second weight operand with GEMM_EPI_B_DUAL, B's type */
+    /* Per-tensor dequantisation factors, device fp32 scalars or NULL (= 1):
+     * the accumulator the program starts from is
+     * (*a_scale_inv) * (*b_scale_inv) * (A @ B), the product taken in fp32.
+     * For an FP8 operand quantised as code = fp8(x * s) this is 1/s; reading
+     * it from device memory lets a scale derived from a previous AMAX feed
+     * the next GEMM without a host round trip.  Any operand type. */
+    const float *a_scale_inv;
+    const float *b_scale_inv;
 } gemm_epi_args;
 
 /* Test hook: the producer skips the first operand load of the first CTA so

@@ -91,25 +91,41 @@ def check_cols(got: np.ndarray, ref: np.ndarray, abs_sum: np.ndarray):
 
 # ------------------------------------------------------------------ running
 
+def operand_host(t: torch.Tensor, in_type: str) -> np.ndarray:
+    """Host copy of an operand as the oracle reads it: bf16 bit patterns or
+    FP8 codes."""
+    if t is None:
+        return None
+    return bits(t) if in_type == "bf16" else t.detach().contiguous().cpu().numpy()
+
+
+def scalar(t):
+    return 1.0 if t is None else float(t.item())
+
+
 def oracle_problem(w: synth.Workload, inp: synth.Inputs) -> oracle.Problem:
     prog = list(w.program)
     aux = bits(inp.aux) if inp.aux is not None else None
     return oracle.Problem(
-        A=bits(inp.A), B=bits(inp.B), program=prog, b_is_nk=(w.b_layout == "nk"),
+        A=operand_host(inp.A, w.in_type), B=operand_host(inp.B, w.in_type), program=prog,
+        b_is_nk=(w.b_layout == "nk"),
         alpha=inp.alpha, bias=None if inp.bias is None else inp.bias.detach().cpu().numpy(),
         residual=aux if w.aux == "residual" else None,
         preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
-        B2=bits(inp.B2) if inp.B2 is not None else None)
+        B2=operand_host(inp.B2, w.in_type), a_type=w.in_type, b_type=w.in_type,
+        a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv))
 
 
 def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
-    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, a_type=w.in_type,
+                    b_type=w.in_type)
     out = api.allocate_outputs(plan, inp.A.device)
     scratch = None
     if unfused:
         scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=inp.A.device)
     api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
-                    bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, B2=inp.B2, **kw)
+                    bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, B2=inp.B2,
+                    a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv, **kw)
     torch.cuda.synchronize()
     status = plan.query_status(out.workspace)
     assert status == 0, "kernel status %d" % status

@@ -39,10 +39,28 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == {s[0] for s in N.SIGNATURES}
 
 
-def test_struct_layouts_match_header(lib):
-    assert ctypes.sizeof(N.gemm_epi_op) == 12
-    assert ctypes.sizeof(N.gemm_epi_desc) == 8 * 8 + 4 + 4 + 8 + 6 * 8
-    assert ctypes.sizeof(N.gemm_epi_args) == 2 * 8 + 2 * 4 + 10 * 8 + 8 + 2 * 4 + 8
+def test_struct_layouts_match_header(lib, tmp_path):
+    """Size and every field offset of the three structs, as a C compiler lays
+    them out from the header, against the ctypes binding."""
+    structs = [N.gemm_epi_op, N.gemm_epi_desc, N.gemm_epi_args]
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "gemm_epi.h"', "int main(void) {"]
+    for st in structs:
+        name = st.__name__
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (name, name))
+        for f, _ in st._fields_:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (name, f, name, f))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for st in structs:
+        name = st.__name__
+        assert int(got[name]) == ctypes.sizeof(st), name
+        for f, _ in st._fields_:
+            assert int(got["%s.%s" % (name, f)]) == getattr(st, f).offset, (name, f)
 
 
 def test_version_and_status_strings(lib):
@@ -64,6 +82,7 @@ def create(lib, M=256, N_=512, K=128, program=("store_bf16",), layout=N.GEMM_EPI
     d.ldc8 = strides.get("ldc8", n_out)
     d.ld_aux = strides.get("ld_aux", n_out)
     d.b_layout = layout
+    d.a_type, d.b_type = strides.get("a_type", 0), strides.get("b_type", 0)
     d.n_ops = strides.get("n_ops", len(program))
     d.ops = ctypes.cast(ops, ctypes.POINTER(N.gemm_epi_op))
     h = N.gemm_epi_handle()
@@ -87,6 +106,14 @@ def test_create_accepts_programs(lib, program):
     assert lib.gemm_epi_out_cols(h) == (256 if pair else 512)
     ws = lib.gemm_epi_workspace_size(h)
     assert ws >= 256 and ws % 256 == 0
+    assert lib.gemm_epi_destroy(h) == N.GEMM_EPI_OK
+
+
+@pytest.mark.parametrize("types", [(1, 1), (1, 2), (2, 1), (2, 2)])
+def test_create_accepts_fp8_operands(lib, types):
+    s, h = create(lib, layout=N.GEMM_EPI_B_NK, a_type=types[0], b_type=types[1], K=144, lda=160, ldb=176,
+                  program=("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"))
+    assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
     assert lib.gemm_epi_destroy(h) == N.GEMM_EPI_OK
 
 
@@ -118,6 +145,14 @@ def test_create_accepts_programs(lib, program):
      N.GEMM_EPI_ERR_INVALID_VALUE),                                      # group must be 128
     (dict(program=("bias", "pair_swiglu:128", "store_bf16")), N.GEMM_EPI_ERR_UNSUPPORTED),
     (dict(layout=N.GEMM_EPI_B_NK | 32, program=("store_bf16",)), N.GEMM_EPI_ERR_INVALID_VALUE),
+    # 8-bit operands
+    (dict(a_type=3), N.GEMM_EPI_ERR_INVALID_VALUE),                      # unknown type
+    (dict(layout=N.GEMM_EPI_B_NK, a_type=1), N.GEMM_EPI_ERR_UNSUPPORTED),  # FP8 A with bf16 B
+    (dict(layout=N.GEMM_EPI_B_NK, b_type=2), N.GEMM_EPI_ERR_UNSUPPORTED),  # bf16 A with FP8 B
+    (dict(a_type=1, b_type=1), N.GEMM_EPI_ERR_UNSUPPORTED),             # FP8 needs B stored N x K
+    (dict(layout=N.GEMM_EPI_B_NK, a_type=1, b_type=1, K=136, lda=144, ldb=144), N.GEMM_EPI_ERR_MISALIGNED),
+    (dict(layout=N.GEMM_EPI_B_NK, a_type=1, b_type=1, lda=136), N.GEMM_EPI_ERR_MISALIGNED),
+    (dict(layout=N.GEMM_EPI_B_NK, a_type=2, b_type=1, ldb=136), N.GEMM_EPI_ERR_MISALIGNED),
 ])
 
 def test_create_rejects(lib, kw, status):

@@ -42,6 +42,7 @@ SMALL_SHAPES = [
     ("downproj", 384, 1000, 328),   # residual + row RMS across 4 N tiles
     ("backward", 200, 776, 192),    # B stored N x K, gelu' + column sums
     ("swiglu2w", 300, 768, 200),    # separate gate / up weights, 384 output columns
+    ("fp8in", 257, 528, 272),       # e4m3 operands, K tail of 16 (one 16-byte group)
 ]
 
 
@@ -69,9 +70,12 @@ def unfused_oracle(w, inp):
     then the epilogue program applied to that stored tensor (written as the
     oracle's GEMM of the stored tensor with an exact bf16 identity)."""
     p = oracle_problem(w, inp)
-    stored = oracle.Problem(p.A, p.B, ["store_bf16"], b_is_nk=p.b_is_nk).rows()["c_bf16"]
+    stored = oracle.Problem(p.A, p.B, ["store_bf16"], b_is_nk=p.b_is_nk, a_type=p.a_type, b_type=p.b_type,
+                            a_scale_inv=p.a_scale_inv, b_scale_inv=p.b_scale_inv).rows()["c_bf16"]
     eye = oracle.to_bf16_bits(np.eye(w.N))
     p.A, p.B, p.b_is_nk = stored, eye, False
+    p.a_type = p.b_type = "bf16"
+    p.a_scale_inv = p.b_scale_inv = 1.0
     return p
 
 
@@ -359,7 +363,7 @@ def test_graph_capture_replay_matches_eager():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w"]
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in"]
 
 
 @pytest.mark.parametrize("name", FULL)
