@@ -131,8 +131,6 @@ struct KernelParams {
   int32_t dual;  // 1: accumulator columns alternate between B and B2 in 128-column blocks
   int32_t a_batched, b_batched;  // operand advances with the batch (else shared)
   int32_t row_blocks;            // row counters per batch
-  int32_t in8;                   // 1: 8-bit operands (kind::f8f6f4), a K block holds 128 elements
-  int32_t k_step;                // elements of K per block: 64 (bf16) or 128 (8-bit)
   const float* a_scale_inv;      // dequantisation factors (F_DEQ), NULL = 1
   const float* b_scale_inv;
   int64_t bs_c, bs_c8, bs_aux;   // batch strides for direct accesses (elements; bytes for C8)
@@ -479,7 +477,10 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 
 // ------------------------------------------------------------------ kernel
 
-template <int CG, class Prog>
+// IN8 = 1: 8-bit operands (tcgen05 kind::f8f6f4); a K block is still one
+// 128-byte swizzle row per operand, now 128 elements.  The operand width is a
+// compile-time choice: a kernel issues MMAs of one kind only.
+template <int CG, class Prog, int IN8 = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tm_a,
                                const __grid_constant__ CUtensorMap tm_b,
@@ -490,6 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using L = Smem<CG>;
   constexpr int STAGES = L::STAGES;
   constexpr int TILE_M = BLOCK_M * CG;  // rows of one tile (the whole CTA group)
+  constexpr int K_STEP = IN8 ? 2 * BLOCK_K : BLOCK_K;  // K elements per stage
   constexpr uint32_t BAR_FULL = L::BAR_FULL, BAR_EMPTY = L::BAR_EMPTY, BAR_TFULL = L::BAR_TFULL,
                      BAR_TEMPTY = L::BAR_TEMPTY, BAR_DRAIN = L::BAR_DRAIN;
   extern __shared__ uint8_t smem_raw[];
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
             if (CG == 1) {
               ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + L::B_STAGE_BYTES);
-              ptx::tma_load_3d(sa, &tm_a, fb, kb * p.k_step, a_row, za);
+              ptx::tma_load_3d(sa, &tm_a, fb, kb * K_STEP, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j) {
@@ -583,23 +585,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
               } else if (p.dual) {
                 // two 128-row K-major boxes, one per operand, stacked in the stage
-                ptx::tma_load_3d(sb, &tm_b, fb, kb * p.k_step, b_col, zb);
-                ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * p.k_step, b_col, zb);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * K_STEP, b_col, zb);
+                ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * K_STEP, b_col, zb);
               } else {
-                ptx::tma_load_3d(sb, &tm_b, fb, kb * p.k_step, b_col, zb);
+                ptx::tma_load_3d(sb, &tm_b, fb, kb * K_STEP, b_col, zb);
               }
             } else {
               // Both CTAs' halves complete on the even CTA's full barrier,
               // which expects the bytes of the whole pair.
               const uint32_t fb0 = ptx::mapa_shared(fb, 0);
               if (rank == 0) ptx::mbar_arrive_expect_tx(fb, 2u * (A_STAGE_BYTES + L::B_STAGE_BYTES));
-              ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * p.k_step, a_row, za);
+              ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * K_STEP, a_row, za);
               if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j)
                   ptx::tma_load_3d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K, zb);
               } else {
-                ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * p.k_step, b_col, zb);
+                ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * K_STEP, b_col, zb);
               }
             }
             issued |= 1u << stage;
@@ -660,13 +662,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
                                        : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-            if (CG == 1) {
-              if (p.in8)
+            if constexpr (CG == 1) {
+              if constexpr (IN8)
                 ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, acc);
               else
                 ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, acc);
             } else {
-              if (p.in8)
+              if constexpr (IN8)
                 ptx::mma_f8_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
               else
                 ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, acc);

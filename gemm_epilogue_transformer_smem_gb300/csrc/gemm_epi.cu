@@ -87,9 +87,12 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
       e = cudaFuncSetAttribute(kDynamic1, cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<1>::BYTES);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kDynamic2, cudaFuncAttributeMaxDynamicSharedMemorySize, ge::Smem<2>::BYTES);
-      for (int t = 0; t < 2 && e == cudaSuccess; ++t) {
-        const ge::KernelSpec* tab = t == 0 ? ge::kSpecsForward : ge::kSpecsAux;
-        const int n = t == 0 ? ge::kNumSpecsForward : ge::kNumSpecsAux;
+      for (int c = 0; c < 2 && e == cudaSuccess; ++c)
+        e = cudaFuncSetAttribute(ge::kDynamicFp8[c], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 c == 0 ? ge::Smem<1>::BYTES : ge::Smem<2>::BYTES);
+      for (int t = 0; t < ge::kNumSpecTables && e == cudaSuccess; ++t) {
+        const ge::KernelSpec* tab = ge::spec_tables()[t].specs;
+        const int n = *ge::spec_tables()[t].n;
         for (int i = 0; i < n && e == cudaSuccess; ++i) {
           e = cudaFuncSetAttribute(tab[i].kernel_1sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    ge::Smem<1>::BYTES);
@@ -334,11 +337,11 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 
   // A compiled kernel whose op list (and pair group) is exactly this one.
   P.spec = nullptr;
-  for (int t = 0; t < 2 && !P.spec; ++t) {
-    const ge::KernelSpec* tab = t == 0 ? ge::kSpecsForward : ge::kSpecsAux;
-    const int n = t == 0 ? ge::kNumSpecsForward : ge::kNumSpecsAux;
+  for (int t = 0; t < ge::kNumSpecTables && !P.spec; ++t) {
+    const ge::KernelSpec* tab = ge::spec_tables()[t].specs;
+    const int n = *ge::spec_tables()[t].n;
     for (int i = 0; i < n && !P.spec; ++i) {
-      if (tab[i].n_ops != d.n_ops) continue;
+      if (tab[i].n_ops != d.n_ops || tab[i].in8 != (P.in8 ? 1 : 0)) continue;
       bool same = true;
       for (int j = 0; j < d.n_ops && same; ++j) {
         const int c = d.ops[j].code;
@@ -378,6 +381,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   L.cg = choose_cta_group(P, a, dev);
   if (P.spec && !(a.debug_flags & GEMM_EPI_DEBUG_FORCE_INTERPRETER))
     L.kernel = L.cg == 2 ? P.spec->kernel_2sm : P.spec->kernel_1sm;
+  else if (P.in8)
+    L.kernel = ge::kDynamicFp8[L.cg == 2 ? 1 : 0];
   else
     L.kernel = L.cg == 2 ? kDynamic2 : kDynamic1;
   const int tile_m = ge::BLOCK_M * L.cg;
@@ -399,9 +404,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.bs_aux = P.batch > 1 ? d.batch_stride_aux : 0;
   // A K block is one 128-byte swizzle row of each operand: 64 bf16 or 128
   // 8-bit elements.
-  k.in8 = P.in8 ? 1 : 0;
-  k.k_step = P.in8 ? 2 * ge::BLOCK_K : ge::BLOCK_K;
-  k.num_k_blocks = static_cast<int32_t>((d.K + k.k_step - 1) / k.k_step);
+  const int k_step = P.in8 ? 2 * ge::BLOCK_K : ge::BLOCK_K;
+  k.num_k_blocks = static_cast<int32_t>((d.K + k_step - 1) / k_step);
   k.group_m = DEFAULT_GROUP_M;
   k.b_kn = (d.b_layout & ~GEMM_EPI_B_DUAL) == GEMM_EPI_B_KN ? 1 : 0;
   k.dual = P.dual ? 1 : 0;
@@ -453,7 +457,7 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   if (d.K > 0) {
     const CUtensorMapDataType op_dt = P.in8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int64_t esz = P.in8 ? 1 : 2;  // bytes per operand element
-    s = make_map(&L.ta, op_dt, a.A, d.K, d.M, d.lda * esz, k.k_step, ge::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B,
+    s = make_map(&L.ta, op_dt, a.A, d.K, d.M, d.lda * esz, k_step, ge::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A", P.batch, k.a_batched ? d.batch_stride_a * esz : 0);
     if (s) return s;
     // Each B operand: N (or N/2 with B2) columns; K-major boxes hold the
@@ -468,7 +472,7 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
                      k.b_batched ? d.batch_stride_b * 2 : 0);
       else
-        s = make_map(map, op_dt, base, d.K, b_cols, d.ldb * esz, k.k_step, nk_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+        s = make_map(map, op_dt, base, d.K, b_cols, d.ldb * esz, k_step, nk_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
                      k.b_batched ? d.batch_stride_b * esz : 0);
       if (s) return s;

@@ -40,28 +40,30 @@ using ProgResidualRms = StaticProgram<GEMM_EPI_OP_ADD_RESIDUAL, GEMM_EPI_OP_STOR
 using ProgGeluGradColSum = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16,
                                          GEMM_EPI_OP_COL_SUM>;
 
-// One compiled program: its op list (code | pair group << 8) and its kernels
-// for the 1-SM and 2-SM main loops.
+// One compiled program: its op list (code | pair group << 8), the operand
+// width it was compiled for and its kernels for the 1-SM and 2-SM main loops.
 struct KernelSpec {
   const char* name;
   int n_ops;
   int ops[GEMM_EPI_MAX_OPS];
+  int in8;  // 1: 8-bit operands
   const void* kernel_1sm;
   const void* kernel_2sm;
 };
 
-template <class Prog, int... Is>
+template <class Prog, int IN8, int... Is>
 inline KernelSpec make_spec(const char* name, std::integer_sequence<int, Is...>) {
   return KernelSpec{name,
                     Prog::n,
                     {(Prog::code_of(Is) | (Prog::arg_of(Is) << 8))...},
-                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<1, Prog>),
-                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<2, Prog>)};
+                    IN8,
+                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<1, Prog, IN8>),
+                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<2, Prog, IN8>)};
 }
 
-template <class Prog>
+template <class Prog, int IN8 = 0>
 inline KernelSpec make_spec(const char* name) {
-  return make_spec<Prog>(name, std::make_integer_sequence<int, Prog::n>{});
+  return make_spec<Prog, IN8>(name, std::make_integer_sequence<int, Prog::n>{});
 }
 
 // Tables defined by the translation units that instantiate the kernels.
@@ -69,5 +71,21 @@ extern const KernelSpec kSpecsForward[];
 extern const int kNumSpecsForward;
 extern const KernelSpec kSpecsAux[];
 extern const int kNumSpecsAux;
+extern const KernelSpec kSpecsFp8[];
+extern const int kNumSpecsFp8;
+// The interpreting kernels for 8-bit operands (1-SM, 2-SM), from the same
+// translation unit as kSpecsFp8.
+extern const void* const kDynamicFp8[2];
+
+struct SpecTable {
+  const KernelSpec* specs;
+  const int* n;
+};
+constexpr int kNumSpecTables = 3;
+inline const SpecTable* spec_tables() {
+  static const SpecTable t[kNumSpecTables] = {
+      {kSpecsForward, &kNumSpecsForward}, {kSpecsAux, &kNumSpecsAux}, {kSpecsFp8, &kNumSpecsFp8}};
+  return t;
+}
 
 }  // namespace ge
