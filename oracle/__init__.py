@@ -9,7 +9,7 @@ codes (uint8) and fp32.
 The program is a list of op names, optionally with one numeric argument:
 ``alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
 gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
-row_rms_unrounded[:eps], col_sum``.
+row_rms_unrounded[:eps], col_sum, dswiglu[:g]``.
 """
 from __future__ import annotations
 
@@ -59,7 +59,7 @@ def load():
         lib.oracle_cols.restype = ctypes.c_int
         lib.oracle_out_cols.argtypes = [P]
         lib.oracle_out_cols.restype = ctypes.c_int
-        for name in ("oracle_gelu_tanh", "oracle_gelu_tanh_grad", "oracle_silu"):
+        for name in ("oracle_gelu_tanh", "oracle_gelu_tanh_grad", "oracle_silu", "oracle_silu_grad"):
             getattr(lib, name).argtypes = [ctypes.c_double]
             getattr(lib, name).restype = ctypes.c_double
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -223,6 +223,10 @@ def gelu_tanh_grad(x: float) -> float:
 
 def silu(x: float) -> float:
     return load().oracle_silu(x)
+
+
+def silu_grad(x: float) -> float:
+    return load().oracle_silu_grad(x)
 
 
 def to_bf16_bits(x) -> np.ndarray:

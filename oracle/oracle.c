@@ -40,6 +40,12 @@
  *  - pair_swiglu(g) / pair_mul(g): output column j takes gate from
  *    accumulator column (j/g)*2g + j%g and up from (j/g)*2g + g + j%g; g = 1
  *    is even/odd.
+ *  - dswiglu(g), the backward of pair_swiglu(g) (CODA's backward epilogues:
+ *    a pairwise transform producing both gradients): the accumulator holds
+ *    dh for h = silu(gate) * up; the forward pre-activations (gate, up) are
+ *    read from `preact` at the same interleaved positions (2N columns), and
+ *    output columns gate(j), up(j) receive dh * up * silu'(gate) and
+ *    dh * silu(gate), silu'(x) = sigmoid(x) (1 + x (1 - sigmoid(x))).
  *  - e4m3 is OCP FP8 E4M3FN (bias 7, max 448, no infinities); quantisation is
  *    round-to-nearest-even of value*scale, saturated to +-448, NaN kept.
  *  - FP8 operands (the FP8 training loop of the cuDNN Graph API tutorial's
@@ -186,13 +192,21 @@ double oracle_gelu_tanh_grad(double x)
 
 double oracle_silu(double x) { return x * sigmoid(x); }
 
+/* d/dx [x sigmoid(x)] = sigmoid(x) (1 + x (1 - sigmoid(x))). */
+double oracle_silu_grad(double x)
+{
+    double s = sigmoid(x);
+    return s * (1.0 + x * (1.0 - s));
+}
+
 /* ------------------------------------------------------------------ */
 /* program parsing                                                     */
 /* ------------------------------------------------------------------ */
 
 enum {
     O_ALPHA, O_BIAS, O_ROW_SCALE, O_RESIDUAL, O_GELU, O_RELU, O_SILU, O_PAIR,
-    O_PAIR_MUL, O_GELU_GRAD, O_AMAX, O_STORE_BF16, O_STORE_E4M3, O_ROW_RMS, O_COL_SUM
+    O_PAIR_MUL, O_GELU_GRAD, O_AMAX, O_STORE_BF16, O_STORE_E4M3, O_ROW_RMS, O_COL_SUM,
+    O_DSWIGLU
 };
 
 typedef struct { int code; double f; int i; } oop;
@@ -212,7 +226,7 @@ static int parse_program(const char *s, oop *ops, int *n_out)
         {"gelu_tanh_grad", O_GELU_GRAD, 0}, {"amax", O_AMAX, 0},
         {"store_bf16", O_STORE_BF16, 0}, {"store_e4m3", O_STORE_E4M3, 0},
         {"row_rms", O_ROW_RMS, 0}, {"row_rms_unrounded", O_ROW_RMS, 1},
-        {"col_sum", O_COL_SUM, 0},
+        {"col_sum", O_COL_SUM, 0}, {"dswiglu", O_DSWIGLU, 0},
     };
     int n = 0;
     const char *p = s ? s : "";
@@ -236,8 +250,9 @@ static int parse_program(const char *s, oop *ops, int *n_out)
         ops[n].f = f;
         ops[n].i = code == O_ROW_RMS ? mode : (int)f;
         /* defaults */
-        if ((code == O_PAIR || code == O_PAIR_MUL) && !has_arg) ops[n].i = 1; /* group g */
-        if ((code == O_PAIR || code == O_PAIR_MUL) && ops[n].i < 1) return -1;
+        if ((code == O_PAIR || code == O_PAIR_MUL || code == O_DSWIGLU) && !has_arg)
+            ops[n].i = 1; /* group g */
+        if ((code == O_PAIR || code == O_PAIR_MUL || code == O_DSWIGLU) && ops[n].i < 1) return -1;
         if (code == O_ROW_RMS && !has_arg) ops[n].f = 1e-6;     /* eps */
         ++n;
     }
@@ -346,14 +361,44 @@ static double apply_elementwise(const oracle_problem *p, const oop *op, double y
     }
 }
 
+static int find_expand(const oop *ops, int n)
+{
+    for (int i = 0; i < n; ++i)
+        if (ops[i].code == O_DSWIGLU) return i;
+    return -1;
+}
+
+/* dswiglu(g): output column o of the 2N columns is the gate or the up
+ * position of one forward pair; it takes accumulator column
+ * j = (o / 2g) g + o % g (the gradient of silu(gate) * up at that pair). */
+static int64_t expand_acc_col(int64_t o, int64_t g)
+{
+    return (o / (2 * g)) * g + o % g;
+}
+
 static void run_elem(const oracle_problem *p, const oop *ops, int nops, int64_t m,
                      int64_t j, double acc_a, double acc_b, elem_out *o)
 {
     int ip = find_pair(ops, nops);
+    int ie = find_expand(ops, nops);
     int first_post = 0;
     double y;
     memset(o, 0, sizeof *o);
-    if (ip >= 0) {
+    if (ie >= 0) {
+        /* j is the output column; acc_a the accumulator at expand_acc_col(j).
+         * Forward: h = silu(gate) * up.  Backward with dh = y:
+         *   d gate = dh * up * silu'(gate),  d up = dh * silu(gate). */
+        int64_t g = ops[ie].i;
+        int64_t jacc = expand_acc_col(j, g);
+        int64_t cg = (j / (2 * g)) * 2 * g + j % g;  /* gate position of the pair */
+        int is_gate = (j % (2 * g)) < g;
+        y = acc_a;
+        for (int i = 0; i < ie; ++i) y = apply_elementwise(p, &ops[i], y, m, jacc);
+        double gate = oracle_bf16_to_double(p->preact[m * p->ld_aux + cg]);
+        double up = oracle_bf16_to_double(p->preact[m * p->ld_aux + cg + g]);
+        y = is_gate ? y * up * oracle_silu_grad(gate) : y * oracle_silu(gate);
+        first_post = ie + 1;
+    } else if (ip >= 0) {
         int64_t g = ops[ip].i;
         int64_t cg = (j / g) * 2 * g + j % g, cu = cg + g;
         double yg = acc_a, yu = acc_b;
@@ -390,6 +435,7 @@ static void run_elem(const oracle_problem *p, const oop *ops, int nops, int64_t 
 
 static int64_t out_cols(const oracle_problem *p, const oop *ops, int n)
 {
+    if (find_expand(ops, n) >= 0) return 2 * p->N;
     return find_pair(ops, n) >= 0 ? p->N / 2 : p->N;
 }
 
@@ -416,6 +462,7 @@ int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
     int nops;
     if (parse_program(p->program, ops, &nops)) return -1;
     int ip = find_pair(ops, nops);
+    int ie = find_expand(ops, nops);
     int64_t nout = out_cols(p, ops, nops);
     double eps = row_rms_eps(ops, nops);
     int bad = 0;
@@ -430,7 +477,9 @@ int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
         double ss = 0.0, am = 0.0;
         for (int64_t j = 0; j < nout; ++j) {
             elem_out o;
-            if (ip >= 0) {
+            if (ie >= 0) {
+                run_elem(p, ops, nops, m, j, acc[expand_acc_col(j, ops[ie].i)], 0.0, &o);
+            } else if (ip >= 0) {
                 int64_t g = ops[ip].i;
                 int64_t cg = (j / g) * 2 * g + j % g;
                 run_elem(p, ops, nops, m, j, acc[cg], acc[cg + g], &o);
@@ -457,6 +506,7 @@ int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
     int nops;
     if (parse_program(p->program, ops, &nops)) return -1;
     int ip = find_pair(ops, nops);
+    int ie = find_expand(ops, nops);
     int64_t nout = out_cols(p, ops, nops);
     int bad = 0;
 
@@ -467,7 +517,9 @@ int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
         double cs = 0.0;
         for (int64_t m = 0; m < p->M; ++m) {
             elem_out o;
-            if (ip >= 0) {
+            if (ie >= 0) {
+                run_elem(p, ops, nops, m, j, acc_elem(p, m, expand_acc_col(j, ops[ie].i)), 0.0, &o);
+            } else if (ip >= 0) {
                 int64_t g = ops[ip].i;
                 int64_t cg = (j / g) * 2 * g + j % g;
                 run_elem(p, ops, nops, m, j, acc_elem(p, m, cg), acc_elem(p, m, cg + g), &o);

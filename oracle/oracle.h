@@ -26,7 +26,8 @@ typedef struct {
     const float *bias;           /* op "bias": one value per column at its point of use */
     const float *row_scale;      /* op "row_scale": M values */
     const uint16_t *residual;    /* op "residual": bf16, M x (columns), row stride ld_aux */
-    const uint16_t *preact;      /* op "gelu_tanh_grad": bf16, same shape and stride */
+    const uint16_t *preact;      /* ops "gelu_tanh_grad" (M x columns) and "dswiglu"
+                                    (M x 2N forward gate/up pairs): bf16, stride ld_aux */
     int64_t ld_aux;
     double fp8_scale;            /* op "store_e4m3": code = e4m3(value * fp8_scale) */
     const char *program;         /* comma-separated op names, optional ":arg" */
@@ -58,6 +59,7 @@ double oracle_e5m2_to_double(uint8_t c);
 double oracle_gelu_tanh(double x);
 double oracle_gelu_tanh_grad(double x);
 double oracle_silu(double x);
+double oracle_silu_grad(double x);
 
 #ifdef __cplusplus
 }

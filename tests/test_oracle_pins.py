@@ -460,3 +460,86 @@ def test_fp8_scale_applies_before_the_program():
 def test_fp8_operand_type_is_enforced():
     with pytest.raises(TypeError):
         Problem(rand_bf16((2, 16)), np.zeros((16, 2), np.uint8), [], a_type="e4m3", b_type="e4m3").rows()
+
+
+# ---------------------------------------------------------------- dSwiGLU
+
+@pytest.mark.parametrize("x", [-20.0, -3.0, -1.0, -0.2, 0.0, 0.3, 1.0, 2.5, 20.0])
+def test_silu_grad_closed_forms(x):
+    d = oracle.silu_grad(x)
+    assert oracle.silu_grad(0.0) == 0.5
+    assert abs(d + oracle.silu_grad(-x) - 1.0) < 1e-14       # silu(x) - silu(-x) = x
+    h = 1e-5
+    fd = (oracle.silu(x + h) - oracle.silu(x - h)) / (2 * h)  # central difference
+    assert abs(d - fd) < 1e-8
+
+
+def _dswiglu_case(M, N, K, g, seed):
+    rng = np.random.default_rng(seed)
+    A = bf16_bits_from_f32(rng.standard_normal((M, K)) * 0.5)
+    B = bf16_bits_from_f32(rng.standard_normal((K, N)) * 0.5)
+    pre = bf16_bits_from_f32(rng.standard_normal((M, 2 * N)) * 1.5)
+    return A, B, pre
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 16])
+def test_dswiglu_matches_autograd(g):
+    """The backward of h = silu(gate) * up by torch autograd (fp64), with dh
+    the GEMM result: both gradients land on the forward's interleaved gate /
+    up positions."""
+    M, N, K = 5, 32, 12
+    A, B, pre = _dswiglu_case(M, N, K, g, 40 + g)
+    y = Problem(A, B, ["dswiglu:%d" % g, "store_bf16"], preact=pre).rows()["y"]
+    P = torch.from_numpy(f64(pre))
+    cols = np.arange(N)
+    cg = (cols // g) * 2 * g + cols % g
+    gate = P[:, cg].clone().requires_grad_(True)
+    up = P[:, cg + g].clone().requires_grad_(True)
+    dh = torch.from_numpy(f64(A) @ f64(B))
+    (torch.nn.functional.silu(gate) * up).backward(dh)
+    ref = np.zeros((M, 2 * N))
+    ref[:, cg] = gate.grad.numpy()
+    ref[:, cg + g] = up.grad.numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_dswiglu_brute_force_with_pre_and_post_ops():
+    """Pure-Python loops: alpha and a row scale on dh (accumulator columns),
+    then bias on the 2N output columns, AMAX, bf16 store and column sums."""
+    M, N, K, g = 3, 8, 6, 2
+    A, B, pre = _dswiglu_case(M, N, K, g, 50)
+    rs = np.array([0.5, 2.0, -1.0], np.float32)
+    bias = np.linspace(-1, 1, 2 * N).astype(np.float32)
+    prog = ["alpha", "row_scale", "dswiglu:2", "bias", "amax", "store_bf16", "col_sum"]
+    p = Problem(A, B, prog, alpha=0.75, row_scale=rs, bias=bias, preact=pre)
+    r = p.rows()
+    c = p.cols(list(range(2 * N)))
+    Af, Bf, Pf = f64(A), f64(B), f64(pre)
+    want = np.zeros((M, 2 * N))
+    for m in range(M):
+        for o in range(2 * N):
+            j = (o // (2 * g)) * g + o % g
+            dh = sum(Af[m, k] * Bf[k, j] for k in range(K)) * 0.75 * float(rs[m])
+            base = (o // (2 * g)) * 2 * g + o % g
+            gt, up = Pf[m, base], Pf[m, base + g]
+            sg = 1.0 / (1.0 + math.exp(-gt))
+            if o % (2 * g) < g:
+                v = dh * up * (sg + gt * sg * (1 - sg))
+            else:
+                v = dh * gt * sg
+            want[m, o] = v + float(bias[o])
+    np.testing.assert_allclose(r["y"], want, rtol=1e-12, atol=1e-13)
+    assert abs(r["amax"] - np.abs(want).max()) < 1e-12
+    np.testing.assert_allclose(c["col_stat"], want.sum(0), rtol=1e-12, atol=1e-12)
+
+
+def test_dswiglu_swapped_gate_up_is_caught():
+    """Swapping the gate and up inputs changes the result, so the autograd
+    pin above would catch it."""
+    M, N, K = 2, 4, 4
+    A, B, pre = _dswiglu_case(M, N, K, 1, 60)
+    swapped = pre.copy()
+    swapped[:, 0::2], swapped[:, 1::2] = pre[:, 1::2], pre[:, 0::2]
+    y1 = Problem(A, B, ["dswiglu", "store_bf16"], preact=pre).rows()["y"]
+    y2 = Problem(A, B, ["dswiglu", "store_bf16"], preact=swapped).rows()["y"]
+    assert np.abs(y1 - y2).max() > 1e-3
