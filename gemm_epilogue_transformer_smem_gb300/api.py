@@ -7,7 +7,7 @@ colon):
 
   alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
   gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
-  row_rms_unrounded[:eps], col_sum
+  row_rms_unrounded[:eps], col_sum, dswiglu[:g]
 """
 from __future__ import annotations
 
@@ -29,6 +29,7 @@ PROGRAM_OPS = {
     "silu": N.GEMM_EPI_OP_ACT_SILU,
     "pair_swiglu": N.GEMM_EPI_OP_PAIR_SWIGLU,
     "pair_mul": N.GEMM_EPI_OP_PAIR_MUL,
+    "dswiglu": N.GEMM_EPI_OP_DSWIGLU,
     "gelu_tanh_grad": N.GEMM_EPI_OP_MUL_GELU_TANH_GRAD,
     "amax": N.GEMM_EPI_OP_AMAX,
     "store_bf16": N.GEMM_EPI_OP_STORE_BF16,
@@ -47,7 +48,7 @@ def encode_program(program: Sequence[str]):
             raise ValueError("unknown epilogue op %r" % name)
         code = PROGRAM_OPS[name]
         i0, f0 = 0, 0.0
-        if name in ("pair_swiglu", "pair_mul"):
+        if name in ("pair_swiglu", "pair_mul", "dswiglu"):
             i0 = int(arg) if arg else 1
         elif name.startswith("row_rms"):
             f0 = float(arg) if arg else 1e-6
@@ -65,6 +66,14 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 OPERAND_TYPES = {"bf16": N.GEMM_EPI_TYPE_BF16, "e4m3": N.GEMM_EPI_TYPE_E4M3, "e5m2": N.GEMM_EPI_TYPE_E5M2}
 
 
+def out_cols(program: Sequence[str], N_: int) -> int:
+    """Output columns of a program over N accumulator columns."""
+    names = [op.partition(":")[0] for op in program]
+    if "dswiglu" in names:
+        return 2 * N_
+    return N_ // 2 if any(n.startswith("pair_") for n in names) else N_
+
+
 class Plan:
     """One validated GEMM + epilogue plan (gemm_epi_create).  Strides default
     to tight row-major packing."""
@@ -80,8 +89,7 @@ class Plan:
         self.program = list(program)
         self.M, self.N, self.K = M, N_, K
         self.b_layout = b_layout
-        pair = any(op.startswith("pair_") for op in program)
-        n_out = N_ // 2 if pair else N_
+        n_out = out_cols(program, N_)
         self._ops = encode_program(program)
         d = N.gemm_epi_desc()
         d.M, d.N, d.K = M, N_, K
@@ -187,7 +195,7 @@ def run_program(plan: Plan, A, B, out: Outputs, *, alpha=1.0, fp8_scale=1.0, bia
     """Runs the plan with the auxiliary tensor routed to residual or preact."""
     prog = [op.partition(":")[0] for op in plan.program]
     residual = aux if "residual" in prog else None
-    preact = aux if "gelu_tanh_grad" in prog else None
+    preact = aux if ("gelu_tanh_grad" in prog or "dswiglu" in prog) else None
     tensors = dict(alpha=alpha, fp8_scale=fp8_scale, bias=bias, row_scale=row_scale,
                    residual=residual, preact=preact, C=out.C, C8=out.C8, amax=out.amax,
                    row_out=out.row_out, col_out=out.col_out, workspace=out.workspace, **kw)

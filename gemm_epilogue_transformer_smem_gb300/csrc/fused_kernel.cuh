@@ -140,6 +140,8 @@ struct KernelParams {
   int32_t pair_at;  // index of PAIR_SWIGLU in ops, or -1
   int32_t pair_g;
   int32_t pair_silu;  // 1: SwiGLU pair, 0: plain product
+  int32_t expand_at;  // index of DSWIGLU in ops, or -1
+  int32_t expand_g;   // its group
   float alpha, fp8_scale, rms_eps;
   int32_t rms_unrounded;
   const float* bias;
@@ -195,6 +197,14 @@ struct StaticProgram {
   static constexpr int pair_g() {
     return pair_at() < 0 ? 1 : (arg_of(pair_at()) == 0 ? 1 : arg_of(pair_at()));
   }
+  static constexpr int expand_at() {
+    for (int i = 0; i < n; ++i)
+      if (code_of(i) == GEMM_EPI_OP_DSWIGLU) return i;
+    return -1;
+  }
+  static constexpr int expand_g() {
+    return expand_at() < 0 ? 1 : (arg_of(expand_at()) == 0 ? 1 : arg_of(expand_at()));
+  }
   static constexpr bool has(int code) {
     for (int i = 0; i < n; ++i)
       if (code_of(i) == code) return true;
@@ -222,6 +232,23 @@ __host__ __device__ constexpr int prog_pair_g() {
   if constexpr (Prog::is_static) return Prog::pair_g(); else return 1;
 }
 template <class Prog>
+__host__ __device__ constexpr int prog_expand_at() {
+  if constexpr (Prog::is_static) return Prog::expand_at(); else return -1;
+}
+template <class Prog>
+__host__ __device__ constexpr int prog_expand_g() {
+  if constexpr (Prog::is_static) return Prog::expand_g(); else return 1;
+}
+// First op applied to output columns: after the pair or expanding op.
+template <class Prog>
+__host__ __device__ constexpr int prog_post_begin() {
+  if constexpr (Prog::is_static) {
+    return Prog::pair_at() >= 0 ? Prog::pair_at() + 1 : Prog::expand_at() >= 0 ? Prog::expand_at() + 1 : 0;
+  } else {
+    return 0;
+  }
+}
+template <class Prog>
 __host__ __device__ constexpr bool prog_pair_silu() {
   if constexpr (Prog::is_static) {
     return Prog::pair_at() >= 0 && Prog::code_of(Prog::pair_at()) == GEMM_EPI_OP_PAIR_SWIGLU;
@@ -241,7 +268,9 @@ __host__ __device__ constexpr uint32_t static_flags() {
     return 0u;
   } else {
     uint32_t f = 0;
-    if (Prog::has(GEMM_EPI_OP_ADD_RESIDUAL) || Prog::has(GEMM_EPI_OP_MUL_GELU_TANH_GRAD)) f |= F_AUX;
+    if (Prog::has(GEMM_EPI_OP_ADD_RESIDUAL) || Prog::has(GEMM_EPI_OP_MUL_GELU_TANH_GRAD) ||
+        Prog::has(GEMM_EPI_OP_DSWIGLU))
+      f |= F_AUX;
     if (Prog::has(GEMM_EPI_OP_STORE_BF16)) f |= F_STORE;
     if (Prog::has(GEMM_EPI_OP_STORE_E4M3)) f |= F_E8;
     if (Prog::has(GEMM_EPI_OP_AMAX)) f |= F_AMAX;
@@ -435,6 +464,33 @@ __device__ __forceinline__ void pair_combine(const float (&a)[64], float (&out)[
     pair_combine_s<true>(a, out, g);
   else
     pair_combine_s<false>(a, out, g);
+}
+
+// The SwiGLU backward on one 32-column output chunk: dh holds the 16
+// accumulator columns the chunk's pairs come from, x the forward gate / up
+// pre-activations at the chunk's output columns.  For h = silu(gate) * up,
+// output gate(j) = dh[j] * up * silu'(gate), output up(j) = dh[j] * silu(gate),
+// silu'(g) = s (1 + g (1 - s)), s = sigmoid(g); gate(j) = (j/G)*2G + j%G.
+template <int G>
+__device__ __forceinline__ void dswiglu_expand_g(const float (&dh)[16], const float (&x)[32], float (&out)[32]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int gate = (j / G) * 2 * G + (j % G);
+    const float gt = x[gate], up = x[gate + G];
+    const float s = sigmoid_f(gt);
+    out[gate] = dh[j] * up * (s * fmaf(gt, 1.0f - s, 1.0f));
+    out[gate + G] = dh[j] * (gt * s);
+  }
+}
+
+__device__ __forceinline__ void dswiglu_expand(const float (&dh)[16], const float (&x)[32], float (&out)[32], int g) {
+  switch (g) {
+    case 2: dswiglu_expand_g<2>(dh, x, out); break;
+    case 4: dswiglu_expand_g<4>(dh, x, out); break;
+    case 8: dswiglu_expand_g<8>(dh, x, out); break;
+    case 16: dswiglu_expand_g<16>(dh, x, out); break;
+    default: dswiglu_expand_g<1>(dh, x, out); break;
+  }
 }
 
 // This thread's 32 auxiliary bf16 values of row m, columns col0.. (zeros
@@ -707,8 +763,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int pair_at = kStatic ? prog_pair_at<Prog>() : p.pair_at;
     const bool paired = pair_at >= 0;
     const bool pair_g128 = paired && (kStatic ? prog_pair_g<Prog>() == 128 : p.pair_g == 128);
-    const int chunks = paired ? BLOCK_N / 64 : BLOCK_N / CHUNK;
-    const int tile_out_cols = paired ? BLOCK_N / 2 : BLOCK_N;
+    // DSWIGLU expands: each 32-column output chunk comes from 16 accumulator
+    // columns, so a tile has 2 * BLOCK_N output columns.
+    const int expand_at = kStatic ? prog_expand_at<Prog>() : p.expand_at;
+    const bool expand = expand_at >= 0;
+    const int chunks = paired ? BLOCK_N / 64 : expand ? 2 * BLOCK_N / CHUNK : BLOCK_N / CHUNK;
+    const int tile_out_cols = paired ? BLOCK_N / 2 : expand ? 2 * BLOCK_N : BLOCK_N;
     // A static program fixes every flag but the K == 0 one at compile time.
     const uint32_t flags = kStatic ? (p.flags & (F_ZERO_ACC | F_DEQ)) | static_flags<Prog>() : p.flags;
     // Product of the dequantisation factors, in fp32 (1 without F_DEQ).
@@ -719,7 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t e80 = sbase + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     uint8_t* epi0_ptr = smem + L::OFF_EPI + ew * EPI_BUFS * EPI_BUF_BYTES;
     uint8_t* e80_ptr = smem + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
-    const int op_begin = paired ? pair_at + 1 : 0;
+    const int op_begin = paired ? pair_at + 1 : expand ? expand_at + 1 : 0;
 
     uint32_t amax_bits = 0;
     uint32_t gchunk = 0;                 // this warp's running chunk number
@@ -768,7 +828,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float v[32];
 
         // ---- accumulator -> registers (and the pair op)
-        if (!paired) {
+        float dh[16];  // DSWIGLU: the chunk's 16 accumulator columns after the ops before it
+        if (expand) {
+          if (flags & F_ZERO_ACC) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dh[j] = 0.0f;
+          } else {
+            uint32_t r[16];
+            ptx::tmem_ld16_sync(t_row + c * 16, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dh[j] = __uint_as_float(r[j]);
+            if (flags & F_DEQ) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) dh[j] *= deq;
+            }
+          }
+          if constexpr (kStatic) {
+            static_for<0, (prog_expand_at<Prog>() < 0 ? 0 : prog_expand_at<Prog>())>([&](auto I) {
+              apply_pointwise<16>(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}, dh, p,
+                                  nacc0 + c * 16, p.N, rs_m);
+            });
+          } else {
+            for (int i = 0; i < expand_at; ++i) apply_pointwise<16>(p.ops[i].code, dh, p, nacc0 + c * 16, p.N, rs_m);
+          }
+        } else if (!paired) {
           if (flags & F_ZERO_ACC) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
@@ -842,6 +925,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = 0.0f;
+        }
+        if (expand) {  // x holds the forward gate / up pairs of the chunk's output columns
+          if constexpr (kStatic)
+            dswiglu_expand_g<prog_expand_g<Prog>()>(dh, x, v);
+          else
+            dswiglu_expand(dh, x, v, p.expand_g);
         }
 
         // ---- the op program on output columns
@@ -936,7 +1025,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         };
         if constexpr (kStatic) {
-          static_for<(prog_pair_at<Prog>() < 0 ? 0 : prog_pair_at<Prog>() + 1), prog_n<Prog>()>(
+          static_for<prog_post_begin<Prog>(), prog_n<Prog>()>(
               [&](auto I) { run_op(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}); });
         } else {
           for (int i = op_begin; i < p.n_ops; ++i) run_op(p.ops[i].code);

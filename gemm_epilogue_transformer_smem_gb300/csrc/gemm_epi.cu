@@ -179,6 +179,7 @@ struct gemm_epi_plan {
   std::vector<gemm_epi_op> ops;
   int64_t n_out = 0;
   int pair_at = -1, pair_g = 1, pair_silu = 1;
+  int expand_at = -1, expand_g = 1;  // DSWIGLU
   bool dual = false;  // GEMM_EPI_B_DUAL: B columns alternate with B2 in 128-column blocks
   bool in8 = false;   // 8-bit operands (kind::f8f6f4)
   int64_t batch = 1, row_blocks = 0;
@@ -217,18 +218,42 @@ gemm_epi_status validate(gemm_epi_plan& P) {
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "n_ops must be in [0, %d]", GEMM_EPI_MAX_OPS);
   if (d.n_ops > 0 && !d.ops) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ops is NULL");
 
-  int seen[16] = {0};
+  int seen[32] = {0};  // indexed by op code
   for (int i = 0; i < d.n_ops; ++i) {
     const gemm_epi_op& op = d.ops[i];
-    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_PAIR_MUL)
+    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_DSWIGLU)
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: unknown code %d", i, op.code);
     if (is_output_op(op.code) && seen[op.code])
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: output op %d appears twice", i, op.code);
     seen[op.code]++;
     switch (op.code) {
+      case GEMM_EPI_OP_DSWIGLU: {
+        if (P.pair_at >= 0 || P.expand_at >= 0)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "a program has at most one pair op");
+        const int g = op.i0 == 0 ? 1 : op.i0;
+        if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "DSWIGLU group %d not in {1,2,4,8,16}", op.i0);
+        if (P.dual) return fail(GEMM_EPI_ERR_UNSUPPORTED, "DSWIGLU with GEMM_EPI_B_DUAL");
+        if (d.N % g != 0)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "DSWIGLU group %d needs N %% %d == 0", g, g);
+        if (2 * d.N > 0x7FFFFFFF) return fail(GEMM_EPI_ERR_INVALID_VALUE, "DSWIGLU needs 2N < 2^31");
+        for (int j = 0; j < i; ++j)
+          if (!is_pre_pair_op(d.ops[j].code))
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "op %d (code %d) before DSWIGLU is not supported", j,
+                        d.ops[j].code);
+        for (int j = i + 1; j < d.n_ops; ++j)
+          if (d.ops[j].code == GEMM_EPI_OP_ADD_RESIDUAL || d.ops[j].code == GEMM_EPI_OP_MUL_GELU_TANH_GRAD)
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "DSWIGLU reads preact; op %d would need a second "
+                                                  "auxiliary tensor", j);
+        P.expand_at = i;
+        P.expand_g = g;
+        P.uses_preact = true;
+        break;
+      }
       case GEMM_EPI_OP_PAIR_SWIGLU:
       case GEMM_EPI_OP_PAIR_MUL: {
-        if (P.pair_at >= 0) return fail(GEMM_EPI_ERR_INVALID_VALUE, "a program has at most one pair op");
+        if (P.pair_at >= 0 || P.expand_at >= 0)
+          return fail(GEMM_EPI_ERR_INVALID_VALUE, "a program has at most one pair op");
         int g = op.i0 == 0 ? 1 : op.i0;
         if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32 && g != 128)
           return fail(GEMM_EPI_ERR_INVALID_VALUE, "pair group %d not in {1,2,4,8,16,32,128}", op.i0);
@@ -275,7 +300,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
                                           "auxiliary tensors; this build reads one");
   if (P.uses_residual || P.uses_preact) P.flags |= ge::F_AUX;
   if (d.K == 0) P.flags |= ge::F_ZERO_ACC;
-  P.n_out = P.pair_at >= 0 ? d.N / 2 : d.N;
+  P.n_out = P.pair_at >= 0 ? d.N / 2 : P.expand_at >= 0 ? 2 * d.N : d.N;
   if ((P.flags & ge::F_ROW) && P.n_out == 0 && d.M > 0)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT over zero columns is undefined");
 
@@ -346,7 +371,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
       for (int j = 0; j < d.n_ops && same; ++j) {
         const int c = d.ops[j].code;
         const bool pair = c == GEMM_EPI_OP_PAIR_SWIGLU || c == GEMM_EPI_OP_PAIR_MUL;
-        const int enc = c | (pair ? P.pair_g << 8 : 0);
+        const int enc = c | (pair ? P.pair_g << 8 : c == GEMM_EPI_OP_DSWIGLU ? P.expand_g << 8 : 0);
         same = enc == tab[i].ops[j];
       }
       if (same) P.spec = &tab[i];
@@ -424,6 +449,8 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.pair_at = P.pair_at;
   k.pair_g = P.pair_g;
   k.pair_silu = P.pair_silu;
+  k.expand_at = P.expand_at;
+  k.expand_g = P.expand_g;
   k.alpha = a.alpha;
   k.fp8_scale = a.fp8_scale;
   k.rms_eps = P.rms_eps;
@@ -616,6 +643,8 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   if (h->pair_at >= 0 && h->pair_g > 8)
     return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass handles pair groups up to 8");
   if (h->batch > 1) return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass runs single problems");
+  if (h->expand_at >= 0 && h->expand_g > 4)
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "the separate pass handles DSWIGLU groups up to 4");
   DeviceState* dev = nullptr;
   gemm_epi_status s = device_state(&dev, nullptr);
   if (s) return s;
@@ -654,6 +683,8 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   u.pair_at = h->pair_at;
   u.pair_g = h->pair_g;
   u.pair_silu = h->pair_silu;
+  u.expand_at = h->expand_at;
+  u.expand_g = h->expand_g;
   u.n_ops = static_cast<int32_t>(h->ops.size());
   u.flags = h->flags;
   u.alpha = args->alpha;

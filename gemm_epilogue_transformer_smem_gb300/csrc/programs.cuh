@@ -36,6 +36,9 @@ using ProgFp8 = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS_COL,
 // residual + acc, bf16 store, per-row rsqrt(mean square + eps).
 using ProgResidualRms = StaticProgram<GEMM_EPI_OP_ADD_RESIDUAL, GEMM_EPI_OP_STORE_BF16,
                                       GEMM_EPI_OP_ROW_RMS_RSQRT>;
+// SwiGLU backward: both gradients from dh and the forward gate / up pairs.
+constexpr int DSWIGLU_G1 = GEMM_EPI_OP_DSWIGLU | (1 << 8);
+using ProgDSwiGLU = StaticProgram<DSWIGLU_G1, GEMM_EPI_OP_STORE_BF16>;
 // acc * gelu_tanh'(preact), bf16 store, column sums.
 using ProgGeluGradColSum = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16,
                                          GEMM_EPI_OP_COL_SUM>;

@@ -23,6 +23,7 @@ struct UnfusedParams {
   int32_t M, N, n_out;
   int32_t pair_at, pair_g, n_ops;
   int32_t pair_silu;  // 1: SwiGLU pair, 0: plain product
+  int32_t expand_at, expand_g;  // DSWIGLU (groups up to 4), or -1
   uint32_t flags;
   float alpha, fp8_scale, rms_eps;
   int32_t rms_unrounded;
@@ -103,7 +104,8 @@ __global__ void __launch_bounds__(UF_THREADS)
   const int row_base = blockIdx.y * UF_ROWS;
   const int c0 = blockIdx.x * UF_COLS + lane * 8;  // first output column of this thread
   const bool paired = p.pair_at >= 0;
-  const int op_begin = paired ? p.pair_at + 1 : 0;
+  const bool expand = p.expand_at >= 0;
+  const int op_begin = paired ? p.pair_at + 1 : expand ? p.expand_at + 1 : 0;
   const int valid = min(8, p.n_out - c0);
   const bool full = valid == 8;
 
@@ -117,7 +119,20 @@ __global__ void __launch_bounds__(UF_THREADS)
     if (m >= p.M || valid <= 0) continue;
     const float rs = p.row_scale ? __ldg(p.row_scale + m) : 0.0f;
     float v[8];
-    if (!paired) {
+    float dh[4];  // DSWIGLU: the 4 accumulator columns c0/2.. of this thread's 8 outputs
+    if (expand) {
+      const int a0 = c0 / 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dh[j] = a0 + j < p.N ? bf16_bits_to_f(p.acc[m * p.ld_acc + a0 + j]) : 0.0f;
+      for (int k = 0; k < p.expand_at; ++k) {
+        float h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = j < 4 ? dh[j] : 0.0f;
+        uf_pointwise(p.ops[k], h, p, a0, min(p.N, a0 + 4), rs);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dh[j] = h[j];
+      }
+    } else if (!paired) {
       load8_bf16(p.acc + m * p.ld_acc + c0, full, valid, v);
     } else {
       // 8 outputs need 16 accumulator columns starting at the pair block.
@@ -167,6 +182,27 @@ __global__ void __launch_bounds__(UF_THREADS)
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+    if (expand) {
+      // Groups g <= 4 keep whole gate / up pairs inside these 8 outputs
+      // (checked on the host).
+      const int g = p.expand_g;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gate = (j / (2 * g)) * 2 * g + j % g;
+        const int jl = (j / (2 * g)) * g + j % g;
+        float gt = 0.0f, up = 0.0f, d = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q == gate) gt = x[q];
+          if (q == gate + g) up = x[q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q == jl) d = dh[q];
+        const float sg = sigmoid_f(gt);
+        v[j] = (j % (2 * g)) < g ? d * up * (sg * fmaf(gt, 1.0f - sg, 1.0f)) : d * (gt * sg);
+      }
     }
     float row_ss = 0.0f;
     for (int k = op_begin; k < p.n_ops; ++k) {

@@ -52,6 +52,7 @@ GEMM_EPI_OP_STORE_E4M3 = 12
 GEMM_EPI_OP_ROW_RMS_RSQRT = 13
 GEMM_EPI_OP_COL_SUM = 14
 GEMM_EPI_OP_PAIR_MUL = 15
+GEMM_EPI_OP_DSWIGLU = 16
 
 GEMM_EPI_MAX_OPS = 16
 GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1

@@ -22,6 +22,12 @@ them; "N(0, s)" has standard deviation s):
   backward  dX = (dY @ W^T) * gelu_tanh'(preact), column sums of dX.
             dY 8192x4096 N(0,1); W 16384x4096 N(0, 0.02); preact 8192x16384
             N(0,1).
+  dswiglu   the SwiGLU backward of the swiglu workload's MLP: dH = dY @ W_down^T
+            with the gradients of both gate and up written from dH and the
+            forward pre-activations.  dY 8192x4096 N(0,1); W_down stored
+            14336x4096 (N x K) N(0, 0.02); preact (the forward gate / up pairs,
+            interleaved) 8192x28672 N(0, 1.28), the spread of the swiglu
+            workload's own GEMM output (0.02 * sqrt(4096)); out 8192x28672.
   fp8in     the fp8 workload's program on FP8 operands: the next layer of the
             FP8 loop reads the e4m3 activations the fp8 workload emits.
             M = N = K = 8192.  A: e4m3 codes of max(N(0, 0.1), 0) * 112 (the
@@ -71,7 +77,10 @@ class Workload:
 
     @property
     def n_out(self) -> int:
-        return self.N // 2 if any(op.startswith("pair_") for op in self.program) else self.N
+        names = [op.partition(":")[0] for op in self.program]
+        if "dswiglu" in names:
+            return 2 * self.N
+        return self.N // 2 if any(n.startswith("pair_") for n in names) else self.N
 
     @property
     def flops(self) -> int:
@@ -111,6 +120,8 @@ WORKLOADS = {
     "backward": Workload("backward", 4, 8192, 16384, 4096, "nk",
                          ("gelu_tanh_grad", "store_bf16", "col_sum"),
                          a_std=1.0, b_std=0.02, aux="preact"),
+    "dswiglu": Workload("dswiglu", 7, 8192, 14336, 4096, "nk", ("dswiglu", "store_bf16"),
+                        a_std=1.0, b_std=0.02, aux="preact", aux_std=1.28),
     "fp8in": Workload("fp8in", 6, 8192, 8192, 8192, "nk",
                       ("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"),
                       a_std=0.1, b_std=1 / math.sqrt(8192), bias_std=0.1, alpha=0.5,
@@ -140,8 +151,8 @@ def _bias_len(w: Workload) -> int:
     if "bias" not in prog:
         return 0
     ib = prog.index("bias")
-    ip = next((i for i, op in enumerate(prog) if op.startswith("pair_")), None)
-    return w.N if (ip is None or ib < ip) else w.N // 2
+    ip = next((i for i, op in enumerate(prog) if op.startswith("pair_") or op.startswith("dswiglu")), None)
+    return w.N if (ip is None or ib < ip) else w.n_out
 
 
 def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs:

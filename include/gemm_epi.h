@@ -56,10 +56,12 @@
  *    byte per element, so lda, ldb and their batch strides count bytes; B
  *    must be GEMM_EPI_B_NK (K contiguous, the usual N x K weight) and K a
  *    multiple of 16.
- *  - Output columns: N_out = N, or N/2 after GEMM_EPI_OP_PAIR_SWIGLU.
+ *  - Output columns: N_out = N, N/2 after GEMM_EPI_OP_PAIR_SWIGLU / PAIR_MUL,
+ *    2N after GEMM_EPI_OP_DSWIGLU.
  *  - C: M x N_out bf16, row stride ldc >= N_out.  C8: M x N_out e4m3 bytes,
  *    row stride ldc8 >= N_out (bytes).
- *  - residual / preact: M x N_out bf16, row stride ld_aux >= N_out.
+ *  - residual / preact: M x N_out bf16, row stride ld_aux >= N_out (with
+ *    DSWIGLU, preact holds the forward pre-activations, M x 2N).
  *  - bias: fp32, N_out values (N values when the op sits before the pair op).
  *  - row_scale: fp32, M values.  amax: 1 fp32.  row_out: M fp32.
  *    col_out: N_out fp32.
@@ -147,9 +149,22 @@ typedef enum gemm_epi_op_code {
     GEMM_EPI_OP_ROW_RMS_RSQRT = 13,     /* row_out[m] = 1/sqrt(mean_n(v^2) + f0), f0 = eps;
                                            v = bf16_rne(y) when i0 == 0, v = y when i0 == 1 */
     GEMM_EPI_OP_COL_SUM = 14,           /* col_out[n] = sum over m of y                      */
-    GEMM_EPI_OP_PAIR_MUL = 15           /* y'[m,j] = y[m,gate(j)] * y[m,up(j)]: the RMSNorm-MLP's
+    GEMM_EPI_OP_PAIR_MUL = 15,          /* y'[m,j] = y[m,gate(j)] * y[m,up(j)]: the RMSNorm-MLP's
                                            plain up * gate; same groups and N_out as
                                            PAIR_SWIGLU, at most one pair op per program      */
+    GEMM_EPI_OP_DSWIGLU = 16            /* backward of PAIR_SWIGLU: y[m,j] = dh for
+                                           h = silu(gate) * up; gate = preact[m, gate(j)],
+                                           up = preact[m, up(j)] (args.preact, the forward
+                                           pre-activations, M x 2N); writes
+                                           y'[m,gate(j)] = dh * up * silu'(gate),
+                                           y'[m,up(j)] = dh * silu(gate);
+                                           silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).
+                                           i0 = group g in {1,2,4,8,16} (0 means 1), same
+                                           gate(j)/up(j) as PAIR_SWIGLU; N % g == 0;
+                                           N_out = 2N.  Ops before it see the N accumulator
+                                           columns, ops after it the 2N outputs; no other
+                                           op may read preact or residual.  Counts as the
+                                           program's pair op.                               */
 } gemm_epi_op_code;
 
 typedef struct gemm_epi_op {
@@ -234,7 +249,7 @@ gemm_epi_status gemm_epi_destroy(gemm_epi_handle h);
 /* Bytes of device workspace gemm_epi_run needs for this plan (>= 256). */
 size_t gemm_epi_workspace_size(gemm_epi_handle h);
 
-/* Output columns of the plan (N, or N/2 after PAIR_SWIGLU); -1 for NULL. */
+/* Output columns of the plan (N, N/2 after a pair op, 2N after DSWIGLU); -1 for NULL. */
 int64_t gemm_epi_out_cols(gemm_epi_handle h);
 
 /* Enqueues the fused kernel on `stream`.  Checks the device (compute

@@ -74,8 +74,7 @@ def create(lib, M=256, N_=512, K=128, program=("store_bf16",), layout=N.GEMM_EPI
     ops = api.encode_program(list(program))
     d = N.gemm_epi_desc()
     d.M, d.N, d.K = M, N_, K
-    pair = any(p.startswith("pair") for p in program)
-    n_out = N_ // 2 if pair else N_
+    n_out = api.out_cols(list(program), N_)
     d.lda = strides.get("lda", K)
     d.ldb = strides.get("ldb", N_ if layout == N.GEMM_EPI_B_KN else K)
     d.ldc = strides.get("ldc", n_out)
@@ -107,6 +106,16 @@ def test_create_accepts_programs(lib, program):
     ws = lib.gemm_epi_workspace_size(h)
     assert ws >= 256 and ws % 256 == 0
     assert lib.gemm_epi_destroy(h) == N.GEMM_EPI_OK
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
+def test_create_accepts_dswiglu(lib, g):
+    prog = ("alpha", "row_scale", "dswiglu:%d" % g, "bias", "amax", "store_bf16", "col_sum")
+    s, h = create(lib, program=prog, ld_aux=1024)
+    assert s == N.GEMM_EPI_OK, lib.gemm_epi_last_error()
+    assert lib.gemm_epi_out_cols(h) == 1024
+    assert lib.gemm_epi_destroy(h) == N.GEMM_EPI_OK
+    assert api.out_cols(list(prog), 512) == 1024
 
 
 @pytest.mark.parametrize("types", [(1, 1), (1, 2), (2, 1), (2, 2)])
@@ -145,6 +154,16 @@ def test_create_accepts_fp8_operands(lib, types):
      N.GEMM_EPI_ERR_INVALID_VALUE),                                      # group must be 128
     (dict(program=("bias", "pair_swiglu:128", "store_bf16")), N.GEMM_EPI_ERR_UNSUPPORTED),
     (dict(layout=N.GEMM_EPI_B_NK | 32, program=("store_bf16",)), N.GEMM_EPI_ERR_INVALID_VALUE),
+    # SwiGLU backward
+    (dict(program=("dswiglu:32", "store_bf16"), ld_aux=1024), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(N_=500, program=("dswiglu:8", "store_bf16"), ld_aux=1024), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("dswiglu", "residual", "store_bf16"), ld_aux=1024), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("dswiglu", "gelu_tanh_grad", "store_bf16"), ld_aux=1024), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("dswiglu", "pair_swiglu", "store_bf16"), ld_aux=1024), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("store_bf16", "dswiglu"), ld_aux=1024), N.GEMM_EPI_ERR_UNSUPPORTED),
+    (dict(program=("dswiglu", "store_bf16"), ld_aux=1000), N.GEMM_EPI_ERR_INVALID_VALUE),  # ld_aux < 2N
+    (dict(layout=N.GEMM_EPI_B_KN | N.GEMM_EPI_B_DUAL, program=("dswiglu", "store_bf16"), ldb=256, ld_aux=1024),
+     N.GEMM_EPI_ERR_UNSUPPORTED),
     # 8-bit operands
     (dict(a_type=3), N.GEMM_EPI_ERR_INVALID_VALUE),                      # unknown type
     (dict(layout=N.GEMM_EPI_B_NK, a_type=1), N.GEMM_EPI_ERR_UNSUPPORTED),  # FP8 A with bf16 B

@@ -43,6 +43,7 @@ SMALL_SHAPES = [
     ("backward", 200, 776, 192),    # B stored N x K, gelu' + column sums
     ("swiglu2w", 300, 768, 200),    # separate gate / up weights, 384 output columns
     ("fp8in", 257, 528, 272),       # e4m3 operands, K tail of 16 (one 16-byte group)
+    ("dswiglu", 300, 520, 200),     # SwiGLU backward: 1040 output columns, 8-column N tail
 ]
 
 
@@ -363,7 +364,7 @@ def test_graph_capture_replay_matches_eager():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in"]
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -395,3 +396,30 @@ def test_full_size_sampled_parity(name):
         s = c.sum(0)
         bound = 2.0 ** -8 * c.abs().sum(0) + 1e-6
         assert torch.all((out.col_out.double() - s).abs() <= bound)
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("g,layout", [(2, "kn"), (4, "nk"), (8, "kn"), (16, "nk")])
+def test_dswiglu_groups_and_ops(g, layout, variant):
+    """The SwiGLU backward with every group, ops on dh before it (alpha, row
+    scale) and on the 2N outputs after it (bias, AMAX, store, column sums)."""
+    M, N, K = 260, 528, 136
+    gen = torch.Generator(device=DEV).manual_seed(70 + g)
+    A = torch.randn(M, K, generator=gen, device=DEV).to(torch.bfloat16)
+    B = (torch.randn(*((K, N) if layout == "kn" else (N, K)), generator=gen, device=DEV) * 0.1).to(torch.bfloat16)
+    pre = (torch.randn(M, 2 * N, generator=gen, device=DEV) * 1.5).to(torch.bfloat16)
+    rs = torch.rand(M, generator=gen, device=DEV) + 0.5
+    bias = torch.randn(2 * N, generator=gen, device=DEV) * 0.1
+    prog = ["alpha", "row_scale", "dswiglu:%d" % g, "bias", "amax", "store_bf16", "col_sum"]
+    plan = api.Plan(M, N, K, prog, b_layout=layout)
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out, alpha=0.5, row_scale=rs, bias=bias, aux=pre, debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    p = oracle.Problem(bits(A), bits(B), prog, b_is_nk=(layout == "nk"), alpha=0.5, row_scale=rs.cpu().numpy(),
+                       bias=bias.cpu().numpy(), preact=bits(pre))
+    r = p.rows()
+    check_bf16(bits(out.C), r["y"])
+    check_amax(float(out.amax.item()), r["amax"])
+    c = p.cols(list(range(2 * N)))
+    check_cols(out.col_out.cpu().numpy(), c["col_stat"], np.abs(c["y"]).sum(0))
