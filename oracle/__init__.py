@@ -9,7 +9,7 @@ codes (uint8) and fp32.
 The program is a list of op names, optionally with one numeric argument:
 ``alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
 gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
-row_rms_unrounded[:eps], col_sum, dswiglu[:g]``.
+row_rms_unrounded[:eps], col_sum, dswiglu[:g], col_scale, row_dot``.
 """
 from __future__ import annotations
 
@@ -39,6 +39,7 @@ class _Problem(ctypes.Structure):
         ("program", ctypes.c_char_p),
         ("a_type", ctypes.c_int), ("b_type", ctypes.c_int),
         ("a_scale_inv", ctypes.c_double), ("b_scale_inv", ctypes.c_double),
+        ("col_scale", ctypes.c_void_p),
     ]
 
 
@@ -70,6 +71,9 @@ def load():
         lib.oracle_double_to_e4m3.restype = ctypes.c_uint8
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_rmsnorm_backward.argtypes = [ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                                ctypes.c_int64, vp, vp, vp, vp, ctypes.c_int64, vp, vp]
+        lib.oracle_rmsnorm_backward.restype = None
         lib.oracle_e5m2_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e5m2_to_double.restype = ctypes.c_double
         _lib = lib
@@ -135,6 +139,7 @@ class Problem:
     b_type: str = "bf16"
     a_scale_inv: float = 1.0
     b_scale_inv: float = 1.0
+    col_scale: Optional[np.ndarray] = None
 
     def _c(self):
         A = _operand(self.A, self.a_type)
@@ -153,7 +158,8 @@ class Problem:
         rs = _f32(self.row_scale)
         res = _u16(self.residual)
         pre = _u16(self.preact)
-        keep += [bias, rs, res, pre]
+        cs = _f32(self.col_scale)
+        keep += [bias, rs, res, pre, cs]
         aux = res if res is not None else pre
         ld_aux = aux.shape[1] if aux is not None else 0
         prog = ",".join(self.program).encode()
@@ -162,7 +168,7 @@ class Problem:
                      A.ctypes.data, A.shape[1], B.ctypes.data, B.shape[1], _ptr(B2),
                      float(self.alpha), _ptr(bias), _ptr(rs), _ptr(res), _ptr(pre),
                      ld_aux, float(self.fp8_scale), prog, TYPES[self.a_type], TYPES[self.b_type],
-                     float(self.a_scale_inv), float(self.b_scale_inv))
+                     float(self.a_scale_inv), float(self.b_scale_inv), _ptr(cs))
         return p, keep
 
     @property
@@ -211,6 +217,21 @@ class Problem:
         if rc != 0:
             raise ValueError("oracle_cols failed (%d)" % rc)
         return {"y": y, "col_stat": cs}
+
+
+def rmsnorm_backward(dy, x, s, r, w=None, add=None, want_dx=True, want_dw=True):
+    """RMSNorm backward from the row reduction r (see oracle.h): returns
+    (dx, dw) in fp64; dy, x, add are bf16 bit patterns (uint16)."""
+    dy, x, add = _u16(dy), _u16(x), _u16(add)
+    M, N = dy.shape
+    s = _f32(s)
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    w = _f32(w)
+    dx = np.empty((M, N), np.float64) if want_dx else None
+    dw = np.empty(N, np.float64) if want_dw else None
+    load().oracle_rmsnorm_backward(M, N, _ptr(dy), dy.shape[1], _ptr(x), x.shape[1], _ptr(w), _ptr(s), _ptr(r),
+                                   _ptr(add), 0 if add is None else add.shape[1], _ptr(dx), _ptr(dw))
+    return dx, dw
 
 
 def gelu_tanh(x: float) -> float:

@@ -40,6 +40,10 @@
  *  - pair_swiglu(g) / pair_mul(g): output column j takes gate from
  *    accumulator column (j/g)*2g + j%g and up from (j/g)*2g + g + j%g; g = 1
  *    is even/odd.
+ *  - col_scale: y * col_scale[n] (a per-column scaling, e.g. an RMSNorm
+ *    weight); row_dot: row_stat[m] = sum_n y * residual[m, n], the row
+ *    reduction of the RMSNorm backward (the CODA page's reductions on the
+ *    output tile); oracle_rmsnorm_backward finishes dx and dw from it.
  *  - dswiglu(g), the backward of pair_swiglu(g) (CODA's backward epilogues:
  *    a pairwise transform producing both gradients): the accumulator holds
  *    dh for h = silu(gate) * up; the forward pre-activations (gate, up) are
@@ -206,7 +210,7 @@ double oracle_silu_grad(double x)
 enum {
     O_ALPHA, O_BIAS, O_ROW_SCALE, O_RESIDUAL, O_GELU, O_RELU, O_SILU, O_PAIR,
     O_PAIR_MUL, O_GELU_GRAD, O_AMAX, O_STORE_BF16, O_STORE_E4M3, O_ROW_RMS, O_COL_SUM,
-    O_DSWIGLU
+    O_DSWIGLU, O_COL_SCALE, O_ROW_DOT
 };
 
 typedef struct { int code; double f; int i; } oop;
@@ -227,6 +231,7 @@ static int parse_program(const char *s, oop *ops, int *n_out)
         {"store_bf16", O_STORE_BF16, 0}, {"store_e4m3", O_STORE_E4M3, 0},
         {"row_rms", O_ROW_RMS, 0}, {"row_rms_unrounded", O_ROW_RMS, 1},
         {"col_sum", O_COL_SUM, 0}, {"dswiglu", O_DSWIGLU, 0},
+        {"col_scale", O_COL_SCALE, 0}, {"row_dot", O_ROW_DOT, 0},
     };
     int n = 0;
     const char *p = s ? s : "";
@@ -332,6 +337,7 @@ typedef struct {
     uint8_t e4m3;
     double amax;     /* |value| at amax, or 0 */
     double row_sq;   /* square used by row_rms */
+    double row_dot;  /* value * residual at row_dot */
     double col_v;    /* value at col_sum */
 } elem_out;
 
@@ -350,6 +356,7 @@ static double apply_elementwise(const oracle_problem *p, const oop *op, double y
     switch (op->code) {
     case O_ALPHA: return p->alpha * y;
     case O_BIAS: return y + (double)p->bias[col];
+    case O_COL_SCALE: return y * (double)p->col_scale[col];
     case O_ROW_SCALE: return y * (double)p->row_scale[m];
     case O_RESIDUAL: return y + oracle_bf16_to_double(p->residual[m * p->ld_aux + col]);
     case O_GELU: return oracle_gelu_tanh(y);
@@ -427,6 +434,7 @@ static void run_elem(const oracle_problem *p, const oop *ops, int nops, int64_t 
             break;
         }
         case O_COL_SUM: o->col_v = y; break;
+        case O_ROW_DOT: o->row_dot = y * oracle_bf16_to_double(p->residual[m * p->ld_aux + j]); break;
         default: y = apply_elementwise(p, op, y, m, j); break;
         }
     }
@@ -465,6 +473,9 @@ int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
     int ie = find_expand(ops, nops);
     int64_t nout = out_cols(p, ops, nops);
     double eps = row_rms_eps(ops, nops);
+    int has_row_dot = 0;
+    for (int i = 0; i < nops; ++i)
+        if (ops[i].code == O_ROW_DOT) has_row_dot = 1;
     int bad = 0;
 
 #pragma omp parallel for schedule(dynamic, 1)
@@ -474,7 +485,7 @@ int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
         double *acc = (double *)malloc(sizeof(double) * (size_t)(p->N > 0 ? p->N : 1));
         if (!acc) { bad = 1; continue; }
         acc_row(p, m, acc);
-        double ss = 0.0, am = 0.0;
+        double ss = 0.0, am = 0.0, rd = 0.0;
         for (int64_t j = 0; j < nout; ++j) {
             elem_out o;
             if (ie >= 0) {
@@ -490,9 +501,10 @@ int oracle_rows(const oracle_problem *p, const int64_t *rows, int64_t nrows,
             if (c_bf16) c_bf16[r * nout + j] = o.bf16;
             if (c_e4m3) c_e4m3[r * nout + j] = o.e4m3;
             ss += o.row_sq;
+            rd += o.row_dot;
             if (o.amax > am || isnan(o.amax)) am = o.amax;
         }
-        if (row_stat) row_stat[r] = 1.0 / sqrt(ss / (double)nout + eps);
+        if (row_stat) row_stat[r] = has_row_dot ? rd : 1.0 / sqrt(ss / (double)nout + eps);
         if (amax_rows) amax_rows[r] = am;
         free(acc);
     }
@@ -532,4 +544,45 @@ int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
         if (col_stat) col_stat[c] = cs;
     }
     return bad ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* RMSNorm backward (second pass)                                      */
+/* ------------------------------------------------------------------ */
+
+/* The gradient of y = x * S * w, S = (mean_n x^2 + eps)^(-1/2), written out:
+ * dy/dx contributes S w dy directly and, through S, -x S^3 / N times
+ * sum_n w dy x (dS/dx[n] = -S^3 x[n] / N).  "Lean4-TileLang Tensor Program
+ * Superoptimizer", section 3 "RMSNorm" (the forward S and its row
+ * broadcast), taken backward the way the CODA page's backward epilogues
+ * pair an on-chip reduction with the output tile. */
+void oracle_rmsnorm_backward(int64_t M, int64_t N, const uint16_t *dy, int64_t ld_dy,
+                             const uint16_t *x, int64_t ld_x, const float *w, const float *s,
+                             const double *r, const uint16_t *add, int64_t ld_add,
+                             double *dx, double *dw)
+{
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t m = 0; m < M; ++m) {
+            double sm = (double)s[m];
+            double c = sm * sm * sm * r[m] / (double)N;
+            for (int64_t n = 0; n < N; ++n) {
+                double wn = w ? (double)w[n] : 1.0;
+                double g = wn * oracle_bf16_to_double(dy[m * ld_dy + n]);
+                double v = sm * g - oracle_bf16_to_double(x[m * ld_x + n]) * c;
+                if (add) v += oracle_bf16_to_double(add[m * ld_add + n]);
+                dx[m * N + n] = v;
+            }
+        }
+    }
+    if (dw) {
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                acc += oracle_bf16_to_double(dy[m * ld_dy + n]) * oracle_bf16_to_double(x[m * ld_x + n]) *
+                       (double)s[m];
+            dw[n] = acc;
+        }
+    }
 }

@@ -34,6 +34,7 @@ typedef struct {
     int a_type, b_type;          /* ORACLE_BF16 (bit patterns), ORACLE_E4M3, ORACLE_E5M2 (codes) */
     double a_scale_inv;          /* the accumulator is a_scale_inv * b_scale_inv * (A @ B) */
     double b_scale_inv;          /* (1.0 for unscaled operands) */
+    const float *col_scale;      /* op "col_scale": one value per column at its point of use */
 } oracle_problem;
 
 enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1, ORACLE_E5M2 = 2 };
@@ -50,6 +51,18 @@ int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
                 double *y, double *col_stat);
 
 int oracle_out_cols(const oracle_problem *p);
+
+/* RMSNorm backward, finished from the row reduction: for y = x * S * w with
+ * S[m] = 1/sqrt(mean_n x^2 + eps) and upstream gradient dy,
+ *   dx[m,n] = S[m] w[n] dy[m,n] - x[m,n] S[m]^3 r[m] / N (+ add[m,n]),
+ *   r[m]    = sum_n w[n] dy[m,n] x[m,n]           (given),
+ *   dw[n]   = sum_m dy[m,n] x[m,n] S[m].
+ * dy, x, add: bf16 bit patterns with row strides; w NULL means 1; add NULL
+ * means none; dx (M x N) and dw (N) in fp64, either may be NULL. */
+void oracle_rmsnorm_backward(int64_t M, int64_t N, const uint16_t *dy, int64_t ld_dy,
+                             const uint16_t *x, int64_t ld_x, const float *w, const float *s,
+                             const double *r, const uint16_t *add, int64_t ld_add,
+                             double *dx, double *dw);
 
 double oracle_bf16_to_double(uint16_t bits);
 uint16_t oracle_double_to_bf16(double x);

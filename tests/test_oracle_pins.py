@@ -543,3 +543,73 @@ def test_dswiglu_swapped_gate_up_is_caught():
     y1 = Problem(A, B, ["dswiglu", "store_bf16"], preact=pre).rows()["y"]
     y2 = Problem(A, B, ["dswiglu", "store_bf16"], preact=swapped).rows()["y"]
     assert np.abs(y1 - y2).max() > 1e-3
+
+
+# ---------------------------------------------------------------- RMSNorm backward
+
+def _rmsnorm_case(M, D, seed):
+    rng = np.random.default_rng(seed)
+    x = bf16_bits_from_f32(rng.standard_normal((M, D)) * 2.0 + 0.3)
+    dy = bf16_bits_from_f32(rng.standard_normal((M, D)))
+    w = (rng.standard_normal(D) * 0.5 + 1.0).astype(np.float32)
+    return x, dy, w
+
+
+@pytest.mark.parametrize("M,D", [(3, 8), (5, 48)])
+def test_rmsnorm_backward_matches_autograd(M, D):
+    """dy arrives as a GEMM result (dy @ I); the epilogue's col_scale (w) and
+    row_dot (sum w dy x) feed the finishing step; dx and dw equal torch
+    autograd of y = x * (mean x^2 + eps)^(-1/2) * w in fp64."""
+    eps = 1e-6
+    x, dy, w = _rmsnorm_case(M, D, 90 + D)
+    xf = f64(x)
+    S = (1.0 / np.sqrt((xf * xf).mean(1) + eps)).astype(np.float32)
+    eye = bf16_bits_from_f32(np.eye(D))
+    r = Problem(dy, eye, ["store_bf16", "col_scale", "row_dot"], col_scale=w, residual=x).rows()["row_stat"]
+    dx, dw = oracle.rmsnorm_backward(dy, x, S, r, w=w)
+    xt = torch.from_numpy(xf).requires_grad_(True)
+    wt = torch.from_numpy(w.astype(np.float64)).requires_grad_(True)
+    St = torch.from_numpy(S.astype(np.float64))  # the forward's S as stored (fp32)
+    # S as a function of x for autograd, pinned to the stored fp32 value
+    Sx = torch.rsqrt((xt * xt).mean(1) + eps)
+    y = xt * (Sx + (St - Sx).detach())[:, None] * wt
+    y.backward(torch.from_numpy(f64(dy)))
+    # S enters the finishing step as the stored fp32 value (2^-24 relative
+    # from the fp64 one autograd differentiates, cubed in the second term).
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-6, atol=1e-6 * np.abs(dx).max())
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-6, atol=1e-6 * np.abs(dw).max())
+
+
+def test_row_dot_and_col_scale_brute_force():
+    M, N, K = 3, 6, 5
+    rng = np.random.default_rng(95)
+    A = bf16_bits_from_f32(rng.standard_normal((M, K)))
+    B = bf16_bits_from_f32(rng.standard_normal((K, N)))
+    x = bf16_bits_from_f32(rng.standard_normal((M, N)))
+    cs = rng.standard_normal(N).astype(np.float32)
+    r = Problem(A, B, ["alpha", "col_scale", "store_bf16", "row_dot"], alpha=0.5, col_scale=cs,
+                residual=x).rows()
+    Af, Bf, xf = f64(A), f64(B), f64(x)
+    want_y = np.zeros((M, N))
+    want_r = np.zeros(M)
+    for m in range(M):
+        for n in range(N):
+            v = sum(Af[m, k] * Bf[k, n] for k in range(K)) * 0.5 * float(cs[n])
+            want_y[m, n] = v
+            want_r[m] += v * xf[m, n]
+    np.testing.assert_allclose(r["y"], want_y, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["row_stat"], want_r, rtol=1e-12, atol=1e-12)
+
+
+def test_rmsnorm_backward_add_term_and_unit_weight():
+    M, D = 4, 16
+    x, dy, _ = _rmsnorm_case(M, D, 97)
+    add = bf16_bits_from_f32(np.arange(M * D, dtype=np.float64).reshape(M, D) / 64)
+    S = np.full(M, 0.5, np.float32)
+    r = np.linspace(-1, 1, M)
+    dx0, dw0 = oracle.rmsnorm_backward(dy, x, S, r)          # w = 1
+    dx1, _ = oracle.rmsnorm_backward(dy, x, S, r, add=add)
+    np.testing.assert_allclose(dx1 - dx0, f64(add), rtol=0, atol=1e-15)
+    want = 0.5 * f64(dy) - f64(x) * (0.125 * r / D)[:, None]
+    np.testing.assert_allclose(dx0, want, rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(dw0, (f64(dy) * f64(x) * 0.5).sum(0), rtol=1e-14)
