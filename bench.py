@@ -211,7 +211,21 @@ def oracle_problem(w, inp):
                           residual=aux if w.aux == "residual" else None,
                           preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
                           B2=operand(inp.B2), a_type=w.in_type, b_type=w.in_type,
-                          a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv))
+                          a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv),
+                          col_scale=None if inp.col_scale is None else inp.col_scale.cpu().numpy())
+
+
+def oracle_step(w, inp, prob, rows):
+    """One bounded sample of the oracle's step: the listed rows of the GEMM
+    + epilogue, then the workload's second pass on those rows."""
+    import oracle
+    from gemm_epilogue_transformer_smem_gb300 import synth
+    ref = prob.rows(rows)
+    if w.finish == "rmsnorm_backward":
+        idx = rows
+        oracle.rmsnorm_backward(ref["c_bf16"], synth.bf16_bits(inp.aux)[idx], inp.row_stat.cpu().numpy()[idx],
+                                ref["row_stat"], w=inp.col_scale.cpu().numpy())
+    return ref
 
 
 def oracle_rows_sample(w, inp, seconds: float):
@@ -224,7 +238,7 @@ def oracle_rows_sample(w, inp, seconds: float):
     rows = max(1, min(w.M, threads))
     while True:
         t0 = time.perf_counter()
-        prob.rows(list(range(rows)))
+        oracle_step(w, inp, prob, list(range(rows)))
         dt = time.perf_counter() - t0
         if dt >= seconds * 0.5 or rows >= w.M:
             break
@@ -250,10 +264,10 @@ def run_reference(args, world, rank):
     _, rows, threads, _ = oracle_rows_sample(w, inp, per_step)
     prob = oracle_problem(w, inp)
     for _ in range(args.warmup):
-        prob.rows(list(range(rows)))
+        oracle_step(w, inp, prob, list(range(rows)))
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        prob.rows(list(range(rows)))
+        oracle_step(w, inp, prob, list(range(rows)))
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K * args.steps
     value = flops / dt / 1e12
@@ -300,10 +314,18 @@ def run_ours(args, world, rank, local):
     out = api.allocate_outputs(plan, dev)
     stream = torch.cuda.current_stream(dev)
     scales = dict(a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv)
-    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2, **scales)
+    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2,
+              col_scale=inp.col_scale, **scales)
+    fin = make_finish(w, inp, out, dev)
+    launches_per_step = 2 if fin else 1
+
+    def gemm():
+        api.run_program(plan, inp.A, inp.B, out, **kw)
 
     def step():
-        api.run_program(plan, inp.A, inp.B, out, **kw)
+        gemm()
+        if fin:
+            fin()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -319,7 +341,13 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     clocks.mark("begin")
-    seconds = time_steps(step, args.steps, stream)
+    if fin:
+        # The GEMM's own launch time (the roofline's kernel) from events
+        # around each GEMM launch inside the timed loop.
+        seconds, gemm_seconds = time_steps_split(gemm, fin, args.steps, stream)
+    else:
+        seconds = time_steps(step, args.steps, stream)
+        gemm_seconds = None
     torch.cuda.synchronize()
     clocks.mark("end")
     barrier(world)
@@ -328,7 +356,7 @@ def run_ours(args, world, rank, local):
     flops = float(w.flops)
     value = aggregate_value(flops * args.steps, world, seconds) / 1e12
     ms_per_step = seconds / args.steps * 1e3
-    fused_tflops = flops / (seconds / args.steps) / 1e12
+    fused_tflops = flops / ((gemm_seconds if gemm_seconds is not None else seconds) / args.steps) / 1e12
 
     extras = {}
     if not args.no_extras:
@@ -345,6 +373,8 @@ def run_ours(args, world, rank, local):
 
         def unfused_step():
             api.run_program(plan, inp.A, inp.B, out, unfused_scratch=scratch, **kw)
+            if fin:
+                fin()
 
         fns = [("fused", step), ("bare", bare_step), ("unfused", unfused_step)]
         try:
@@ -374,7 +404,7 @@ def run_ours(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(plan, w, inp, out, kw, dev, max(3, min(args.steps, 20)), world)
+        e2e = measure_e2e(plan, w, inp, out, kw, dev, max(3, min(args.steps, 20)), world, fin)
 
     if rank != 0:
         return
@@ -410,14 +440,51 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         **extras,
     }
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
+def make_finish(w, inp, out, dev):
+    """The workload's second pass as a callable (None without one): the
+    RMSNorm backward from the GEMM's stored dy and row reduction."""
+    if w.finish != "rmsnorm_backward":
+        return None
+    import torch
+    from gemm_epilogue_transformer_smem_gb300 import api
+    dx = torch.empty(out.C.shape, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(out.C.shape[1], dtype=torch.float32, device=dev)
+
+    def fin(aux=None, C=None, row_out=None, w_=None, s_=None):
+        api.rmsnorm_backward(out.C if C is None else C, inp.aux if aux is None else aux,
+                             inp.row_stat if s_ is None else s_, out.row_out if row_out is None else row_out,
+                             w=inp.col_scale if w_ is None else w_, dx=dx, dw=dw)
+
+    fin.outputs = (dx, dw)
+    return fin
+
+
+def time_steps_split(first, second, steps, stream):
+    """Times `steps` of first(); second() with events around the whole loop
+    and around each first(); returns (total seconds, seconds in first())."""
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start.record(stream)
+    for a, b in marks:
+        a.record(stream)
+        first()
+        b.record(stream)
+        second()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3, sum(a.elapsed_time(b) for a, b in marks) / 1e3
+
+
+def measure_e2e(plan, w, inp, out, kw, dev, steps, world, fin=None):
     """Same metric through the C ABI with host buffers: every step copies the
     inputs from pinned host memory, runs, and reads the outputs back."""
     import torch
@@ -425,9 +492,12 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
 
     h = {k: (v.cpu().pin_memory() if v is not None else None)
          for k, v in (("A", inp.A), ("B", inp.B), ("bias", inp.bias), ("aux", inp.aux), ("B2", inp.B2),
-                      ("a_scale_inv", inp.a_scale_inv), ("b_scale_inv", inp.b_scale_inv))}
+                      ("a_scale_inv", inp.a_scale_inv), ("b_scale_inv", inp.b_scale_inv),
+                      ("col_scale", inp.col_scale), ("row_stat", inp.row_stat))}
     d = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
     outs = [t for t in (out.C, out.C8, out.amax, out.row_out, out.col_out) if t is not None]
+    if fin:
+        outs += list(fin.outputs)
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
     d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -439,7 +509,9 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world):
                 d[k].copy_(v, non_blocking=True)
         api.run_program(plan, d["A"], d["B"], out, alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
                         bias=d["bias"], aux=d["aux"], B2=d["B2"], a_scale_inv=d["a_scale_inv"],
-                        b_scale_inv=d["b_scale_inv"])
+                        b_scale_inv=d["b_scale_inv"], col_scale=d["col_scale"])
+        if fin:
+            fin(aux=d["aux"], w_=d["col_scale"], s_=d["row_stat"])
         for t, ht in zip(outs, host_out):
             ht.copy_(t, non_blocking=True)
 

@@ -7,7 +7,7 @@ colon):
 
   alpha, bias, row_scale, residual, gelu_tanh, relu, silu, pair_swiglu[:g], pair_mul[:g],
   gelu_tanh_grad, amax, store_bf16, store_e4m3, row_rms[:eps],
-  row_rms_unrounded[:eps], col_sum, dswiglu[:g]
+  row_rms_unrounded[:eps], col_sum, dswiglu[:g], col_scale, row_dot
 """
 from __future__ import annotations
 
@@ -30,6 +30,8 @@ PROGRAM_OPS = {
     "pair_swiglu": N.GEMM_EPI_OP_PAIR_SWIGLU,
     "pair_mul": N.GEMM_EPI_OP_PAIR_MUL,
     "dswiglu": N.GEMM_EPI_OP_DSWIGLU,
+    "col_scale": N.GEMM_EPI_OP_MUL_COL_SCALE,
+    "row_dot": N.GEMM_EPI_OP_ROW_DOT,
     "gelu_tanh_grad": N.GEMM_EPI_OP_MUL_GELU_TANH_GRAD,
     "amax": N.GEMM_EPI_OP_AMAX,
     "store_bf16": N.GEMM_EPI_OP_STORE_BF16,
@@ -64,6 +66,11 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 # Operand element types (desc.a_type / b_type); 8-bit operands are passed as
 # uint8 (or torch float8) tensors of codes.
 OPERAND_TYPES = {"bf16": N.GEMM_EPI_TYPE_BF16, "e4m3": N.GEMM_EPI_TYPE_E4M3, "e5m2": N.GEMM_EPI_TYPE_E5M2}
+
+
+# Ops that read the auxiliary M x N_out tensor, by the argument it travels in.
+RESIDUAL_OPS = frozenset({"residual", "row_dot"})
+PREACT_OPS = frozenset({"gelu_tanh_grad", "dswiglu"})
 
 
 def out_cols(program: Sequence[str], N_: int) -> int:
@@ -129,10 +136,12 @@ class Plan:
 
     def args(self, A, B, *, alpha=1.0, fp8_scale=1.0, bias=None, row_scale=None, residual=None,
              preact=None, C=None, C8=None, amax=None, row_out=None, col_out=None, workspace=None,
-             timeout_ms=0, debug_flags=0, B2=None, a_scale_inv=None, b_scale_inv=None) -> N.gemm_epi_args:
+             timeout_ms=0, debug_flags=0, B2=None, a_scale_inv=None, b_scale_inv=None,
+             col_scale=None) -> N.gemm_epi_args:
         a = N.gemm_epi_args()
         a.A, a.B, a.B2 = _ptr(A), _ptr(B), _ptr(B2)
         a.a_scale_inv, a.b_scale_inv = _ptr(a_scale_inv), _ptr(b_scale_inv)
+        a.col_scale = _ptr(col_scale)
         a.alpha, a.fp8_scale = float(alpha), float(fp8_scale)
         a.bias, a.row_scale = _ptr(bias), _ptr(row_scale)
         a.residual, a.preact = _ptr(residual), _ptr(preact)
@@ -182,7 +191,7 @@ def allocate_outputs(plan: Plan, device) -> Outputs:
         o.C8 = torch.empty(lead + (plan.M, plan.n_out), dtype=torch.uint8, device=device)
     if "amax" in prog:
         o.amax = torch.empty(1, dtype=torch.float32, device=device)
-    if any(p.startswith("row_rms") for p in prog):
+    if any(p.startswith("row_rms") or p == "row_dot" for p in prog):
         o.row_out = torch.empty(lead + (plan.M,), dtype=torch.float32, device=device)
     if "col_sum" in prog:
         o.col_out = torch.empty(lead + (plan.n_out,), dtype=torch.float32, device=device)
@@ -194,8 +203,8 @@ def run_program(plan: Plan, A, B, out: Outputs, *, alpha=1.0, fp8_scale=1.0, bia
                 row_scale=None, aux=None, unfused_scratch=None, **kw) -> Outputs:
     """Runs the plan with the auxiliary tensor routed to residual or preact."""
     prog = [op.partition(":")[0] for op in plan.program]
-    residual = aux if "residual" in prog else None
-    preact = aux if ("gelu_tanh_grad" in prog or "dswiglu" in prog) else None
+    residual = aux if any(op in RESIDUAL_OPS for op in prog) else None
+    preact = aux if any(op in PREACT_OPS for op in prog) else None
     tensors = dict(alpha=alpha, fp8_scale=fp8_scale, bias=bias, row_scale=row_scale,
                    residual=residual, preact=preact, C=out.C, C8=out.C8, amax=out.amax,
                    row_out=out.row_out, col_out=out.col_out, workspace=out.workspace, **kw)
@@ -204,3 +213,20 @@ def run_program(plan: Plan, A, B, out: Outputs, *, alpha=1.0, fp8_scale=1.0, bia
     else:
         plan.run(A, B, **tensors)
     return out
+
+
+def rmsnorm_backward(dy, x, s, r, *, w=None, add=None, dx=None, dw=None, stream=None):
+    """gemm_epi_rmsnorm_backward: dx = S w dy - x S^3 r / N (+ add) into `dx`
+    and dw = sum_m dy x S into `dw` (either may be None); bf16 2-D tensors
+    with unit column stride, fp32 vectors.  Asynchronous."""
+    lib = N.load()
+    a = N.gemm_epi_rmsnorm_bwd_args()
+    a.M, a.N = dy.shape
+    a.dy, a.ld_dy = _ptr(dy), dy.stride(0)
+    a.x, a.ld_x = _ptr(x), x.stride(0)
+    a.add, a.ld_add = _ptr(add), (add.stride(0) if add is not None else 0)
+    a.w, a.s, a.r = _ptr(w), _ptr(s), _ptr(r)
+    a.dx, a.ld_dx = _ptr(dx), (dx.stride(0) if dx is not None else 0)
+    a.dw = _ptr(dw)
+    st = (stream or torch.cuda.current_stream()).cuda_stream
+    N.check(lib.gemm_epi_rmsnorm_backward(ctypes.byref(a), ctypes.c_void_p(st)), lib)

@@ -29,7 +29,7 @@ def sources(csrc=CSRC):
 
 
 def compile_command(src: str, obj: str, extra=()):
-    return ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+    return ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
             "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), *extra,
             "-c", "-o", obj, src]
 

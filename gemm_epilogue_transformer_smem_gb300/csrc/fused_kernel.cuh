@@ -101,6 +101,7 @@ enum : uint32_t {
   F_COL = 1u << 5,
   F_ZERO_ACC = 1u << 6,  // K == 0: the accumulator is zero, TMEM is not read
   F_DEQ = 1u << 7,       // the accumulator is multiplied by the operands' dequantisation factors
+  F_RSQRT = 1u << 8,     // row sums become 1/sqrt(mean + eps) (ROW_RMS_RSQRT; ROW_DOT keeps the sum)
 };
 
 // Where a bounded wait ran out (second status word).
@@ -145,6 +146,7 @@ struct KernelParams {
   float alpha, fp8_scale, rms_eps;
   int32_t rms_unrounded;
   const float* bias;
+  const float* col_scale;
   const float* row_scale;
   float* amax;
   float* row_out;
@@ -269,12 +271,13 @@ __host__ __device__ constexpr uint32_t static_flags() {
   } else {
     uint32_t f = 0;
     if (Prog::has(GEMM_EPI_OP_ADD_RESIDUAL) || Prog::has(GEMM_EPI_OP_MUL_GELU_TANH_GRAD) ||
-        Prog::has(GEMM_EPI_OP_DSWIGLU))
+        Prog::has(GEMM_EPI_OP_DSWIGLU) || Prog::has(GEMM_EPI_OP_ROW_DOT))
       f |= F_AUX;
     if (Prog::has(GEMM_EPI_OP_STORE_BF16)) f |= F_STORE;
     if (Prog::has(GEMM_EPI_OP_STORE_E4M3)) f |= F_E8;
     if (Prog::has(GEMM_EPI_OP_AMAX)) f |= F_AMAX;
-    if (Prog::has(GEMM_EPI_OP_ROW_RMS_RSQRT)) f |= F_ROW;
+    if (Prog::has(GEMM_EPI_OP_ROW_RMS_RSQRT)) f |= F_ROW | F_RSQRT;
+    if (Prog::has(GEMM_EPI_OP_ROW_DOT)) f |= F_ROW;
     if (Prog::has(GEMM_EPI_OP_COL_SUM)) f |= F_COL;
     return f;
   }
@@ -412,6 +415,23 @@ __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], cons
 #pragma unroll
         for (int j = 0; j < NV; ++j)
           if (col0 + j < ncols) v[j] += __ldg(p.bias + col0 + j);
+      }
+      break;
+    case GEMM_EPI_OP_MUL_COL_SCALE:
+      if (col0 + NV <= ncols) {
+        const float4* c4 = reinterpret_cast<const float4*>(p.col_scale + col0);
+#pragma unroll
+        for (int q = 0; q < NV / 4; ++q) {
+          const float4 c = __ldg(c4 + q);
+          v[4 * q + 0] *= c.x;
+          v[4 * q + 1] *= c.y;
+          v[4 * q + 2] *= c.z;
+          v[4 * q + 3] *= c.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < ncols) v[j] *= __ldg(p.col_scale + col0 + j);
       }
       break;
     case GEMM_EPI_OP_MUL_ROW_SCALE:
@@ -1004,6 +1024,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               break;
             }
+            case GEMM_EPI_OP_ROW_DOT:
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (full_cols || col0 + j < p.n_out) row_ss = fmaf(v[j], x[j], row_ss);
+              break;
             case GEMM_EPI_OP_ROW_RMS_RSQRT:
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
@@ -1059,7 +1084,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       // ---- row statistics: partial sums, then the last arriving warp of
       // this row block turns them into 1/sqrt(mean + eps).
-      if (flags & F_ROW) {
+      if ((flags & F_ROW) && !(flags & F_RSQRT)) {
+        // ROW_DOT: the partial sums are the result.
+        if (row_ok) atomicAdd(p.row_out + row_base + m, row_ss);
+      } else if (flags & F_ROW) {
         if (row_ok) atomicAdd(p.row_out + row_base + m, row_ss);
         __threadfence();
         __syncwarp();

@@ -24,6 +24,7 @@
 
 #include "gemm_epi.h"
 #include "programs.cuh"
+#include "rmsnorm_bwd.cuh"
 #include "unfused_kernel.cuh"
 
 namespace {
@@ -58,6 +59,16 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[128];
 
+// Every table of static kernels (internal linkage: each copy of the library
+// in a process keeps its own).
+struct SpecTable {
+  const ge::KernelSpec* specs;
+  const int* n;
+};
+const SpecTable kSpecTables[] = {
+    {ge::kSpecsForward, &ge::kNumSpecsForward}, {ge::kSpecsAux, &ge::kNumSpecsAux}, {ge::kSpecsFp8, &ge::kNumSpecsFp8}};
+constexpr int kNumSpecTables = sizeof(kSpecTables) / sizeof(kSpecTables[0]);
+
 // The interpreting kernels (any program); static ones come from the tables.
 const void* const kDynamic1 = reinterpret_cast<const void*>(&ge::fused_gemm_epilogue_kernel<1, ge::DynamicProgram>);
 const void* const kDynamic2 = reinterpret_cast<const void*>(&ge::fused_gemm_epilogue_kernel<2, ge::DynamicProgram>);
@@ -90,9 +101,9 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
       for (int c = 0; c < 2 && e == cudaSuccess; ++c)
         e = cudaFuncSetAttribute(ge::kDynamicFp8[c], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  c == 0 ? ge::Smem<1>::BYTES : ge::Smem<2>::BYTES);
-      for (int t = 0; t < ge::kNumSpecTables && e == cudaSuccess; ++t) {
-        const ge::KernelSpec* tab = ge::spec_tables()[t].specs;
-        const int n = *ge::spec_tables()[t].n;
+      for (int t = 0; t < kNumSpecTables && e == cudaSuccess; ++t) {
+        const ge::KernelSpec* tab = kSpecTables[t].specs;
+        const int n = *kSpecTables[t].n;
         for (int i = 0; i < n && e == cudaSuccess; ++i) {
           e = cudaFuncSetAttribute(tab[i].kernel_1sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    ge::Smem<1>::BYTES);
@@ -168,7 +179,8 @@ bool is_output_op(int c) {
 }
 
 bool is_pre_pair_op(int c) {
-  return c == GEMM_EPI_OP_SCALE_ALPHA || c == GEMM_EPI_OP_ADD_BIAS_COL || c == GEMM_EPI_OP_MUL_ROW_SCALE ||
+  return c == GEMM_EPI_OP_SCALE_ALPHA || c == GEMM_EPI_OP_ADD_BIAS_COL || c == GEMM_EPI_OP_MUL_COL_SCALE ||
+         c == GEMM_EPI_OP_MUL_ROW_SCALE ||
          c == GEMM_EPI_OP_ACT_GELU_TANH || c == GEMM_EPI_OP_ACT_RELU || c == GEMM_EPI_OP_ACT_SILU;
 }
 
@@ -185,6 +197,7 @@ struct gemm_epi_plan {
   int64_t batch = 1, row_blocks = 0;
   uint32_t flags = 0;
   bool uses_bias = false, uses_row_scale = false, uses_residual = false, uses_preact = false;
+  bool uses_col_scale = false;
   float rms_eps = 0.0f;
   int rms_unrounded = 0;
   int64_t num_m_tiles = 0, num_n_tiles = 0;
@@ -221,7 +234,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   int seen[32] = {0};  // indexed by op code
   for (int i = 0; i < d.n_ops; ++i) {
     const gemm_epi_op& op = d.ops[i];
-    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_DSWIGLU)
+    if (op.code < GEMM_EPI_OP_SCALE_ALPHA || op.code > GEMM_EPI_OP_ROW_DOT)
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: unknown code %d", i, op.code);
     if (is_output_op(op.code) && seen[op.code])
       return fail(GEMM_EPI_ERR_INVALID_VALUE, "op %d: output op %d appears twice", i, op.code);
@@ -268,8 +281,8 @@ gemm_epi_status validate(gemm_epi_plan& P) {
                         d.ops[j].code);
           // Group 128 pairs columns 128 apart within a tile, so a column bias
           // before it would have to follow that layout; not offered.
-          if (g == 128 && d.ops[j].code == GEMM_EPI_OP_ADD_BIAS_COL)
-            return fail(GEMM_EPI_ERR_UNSUPPORTED, "ADD_BIAS_COL before a pair op of group 128");
+          if (g == 128 && (d.ops[j].code == GEMM_EPI_OP_ADD_BIAS_COL || d.ops[j].code == GEMM_EPI_OP_MUL_COL_SCALE))
+            return fail(GEMM_EPI_ERR_UNSUPPORTED, "a column vector before a pair op of group 128");
         }
         P.pair_at = i;
         P.pair_g = g;
@@ -282,8 +295,13 @@ gemm_epi_status validate(gemm_epi_plan& P) {
         if (op.i0 != 0 && op.i0 != 1) return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT mode must be 0 or 1");
         P.rms_eps = op.f0;
         P.rms_unrounded = op.i0;
-        P.flags |= ge::F_ROW;
+        P.flags |= ge::F_ROW | ge::F_RSQRT;
         break;
+      case GEMM_EPI_OP_ROW_DOT:
+        P.flags |= ge::F_ROW;
+        P.uses_residual = true;
+        break;
+      case GEMM_EPI_OP_MUL_COL_SCALE: P.uses_col_scale = true; break;
       case GEMM_EPI_OP_ADD_BIAS_COL: P.uses_bias = true; break;
       case GEMM_EPI_OP_MUL_ROW_SCALE: P.uses_row_scale = true; break;
       case GEMM_EPI_OP_ADD_RESIDUAL: P.uses_residual = true; break;
@@ -296,12 +314,14 @@ gemm_epi_status validate(gemm_epi_plan& P) {
     }
   }
   if (P.uses_residual && P.uses_preact)
-    return fail(GEMM_EPI_ERR_UNSUPPORTED, "ADD_RESIDUAL and MUL_GELU_TANH_GRAD in one program need two "
+    return fail(GEMM_EPI_ERR_UNSUPPORTED, "ops reading residual and ops reading preact in one program need two "
                                           "auxiliary tensors; this build reads one");
   if (P.uses_residual || P.uses_preact) P.flags |= ge::F_AUX;
   if (d.K == 0) P.flags |= ge::F_ZERO_ACC;
   P.n_out = P.pair_at >= 0 ? d.N / 2 : P.expand_at >= 0 ? 2 * d.N : d.N;
-  if ((P.flags & ge::F_ROW) && P.n_out == 0 && d.M > 0)
+  if (seen[GEMM_EPI_OP_ROW_DOT] && seen[GEMM_EPI_OP_ROW_RMS_RSQRT])
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_DOT and ROW_RMS_RSQRT both write row_out");
+  if ((P.flags & ge::F_RSQRT) && P.n_out == 0 && d.M > 0)
     return fail(GEMM_EPI_ERR_INVALID_VALUE, "ROW_RMS_RSQRT over zero columns is undefined");
 
   // Strides: bounds first, then the 16-byte TMA rule.
@@ -362,9 +382,9 @@ gemm_epi_status validate(gemm_epi_plan& P) {
 
   // A compiled kernel whose op list (and pair group) is exactly this one.
   P.spec = nullptr;
-  for (int t = 0; t < ge::kNumSpecTables && !P.spec; ++t) {
-    const ge::KernelSpec* tab = ge::spec_tables()[t].specs;
-    const int n = *ge::spec_tables()[t].n;
+  for (int t = 0; t < kNumSpecTables && !P.spec; ++t) {
+    const ge::KernelSpec* tab = kSpecTables[t].specs;
+    const int n = *kSpecTables[t].n;
     for (int i = 0; i < n && !P.spec; ++i) {
       if (tab[i].n_ops != d.n_ops || tab[i].in8 != (P.in8 ? 1 : 0)) continue;
       bool same = true;
@@ -456,6 +476,7 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
   k.rms_eps = P.rms_eps;
   k.rms_unrounded = P.rms_unrounded;
   k.bias = a.bias;
+  k.col_scale = a.col_scale;
   k.row_scale = a.row_scale;
   k.amax = a.amax;
   k.row_out = a.row_out;
@@ -535,6 +556,7 @@ gemm_epi_status check_args(const gemm_epi_plan& P, const gemm_epi_args& a) {
     if ((P.flags & ge::F_STORE) && (s = need(a.C, "C"))) return s;
     if ((P.flags & ge::F_E8) && (s = need(a.C8, "C8"))) return s;
     if (P.uses_bias && (s = need(a.bias, "bias"))) return s;
+    if (P.uses_col_scale && (s = need(a.col_scale, "col_scale"))) return s;
     if (P.uses_row_scale && (s = need(a.row_scale, "row_scale"))) return s;
     if (P.uses_residual && (s = need(a.residual, "residual"))) return s;
     if (P.uses_preact && (s = need(a.preact, "preact"))) return s;
@@ -624,10 +646,10 @@ int64_t gemm_epi_out_cols(gemm_epi_handle h) { return h ? h->n_out : -1; }
 gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args* args, void* stream) {
   g_last_error.clear();
   if (!h || !args) return fail(GEMM_EPI_ERR_INVALID_VALUE, "handle and args must not be NULL");
-  DeviceState* dev = nullptr;
-  gemm_epi_status s = device_state(&dev, nullptr);
+  gemm_epi_status s = check_args(*h, *args);  // host-only checks first
   if (s) return s;
-  if ((s = check_args(*h, *args))) return s;
+  DeviceState* dev = nullptr;
+  if ((s = device_state(&dev, nullptr))) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = clear_outputs(*h, *args, st))) return s;
   if (h->d.M == 0 || h->n_out == 0) return GEMM_EPI_OK;
@@ -696,6 +718,7 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   u.aux = static_cast<const uint16_t*>(h->uses_residual ? args->residual : args->preact);
   u.ld_aux = d.ld_aux;
   u.bias = args->bias;
+  u.col_scale = args->col_scale;
   u.row_scale = args->row_scale;
   u.c = static_cast<uint16_t*>(args->C);
   u.ldc = d.ldc;
@@ -715,7 +738,7 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   ge::unfused_epilogue_kernel<<<grid, ge::UF_THREADS, 0, st>>>(u);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the separate epilogue pass");
-  if (h->flags & ge::F_ROW) {
+  if ((h->flags & ge::F_ROW) && (h->flags & ge::F_RSQRT)) {
     const int threads = 256;
     ge::row_rms_finalize_kernel<<<static_cast<unsigned>((d.M + threads - 1) / threads), threads, 0, st>>>(
         args->row_out, static_cast<int>(d.M), 1.0f / static_cast<float>(h->n_out), h->rms_eps);
@@ -765,6 +788,65 @@ gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args* ar
   Launch L;
   if ((s = prepare(*h, a, *dev, L))) return s;
   return launch_fused(L, st);
+}
+
+gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bwd_args* a, void* stream) {
+  g_last_error.clear();
+  if (!a) return fail(GEMM_EPI_ERR_INVALID_VALUE, "args must not be NULL");
+  if (a->M < 0 || a->N < 0 || a->M > 0x7FFFFFFF || a->N > 0x7FFFFFFF)
+    return fail(GEMM_EPI_ERR_INVALID_VALUE, "M, N must be in [0, 2^31)");
+  gemm_epi_status s;
+  if (a->dw && (reinterpret_cast<uintptr_t>(a->dw) & 3u))
+    return fail(GEMM_EPI_ERR_MISALIGNED, "dw must be 4-byte aligned");
+  const bool work = a->M > 0 && a->N > 0 && (a->dx || a->dw);
+  auto tensor = [&](const void* ptr, int64_t ld, const char* name) -> gemm_epi_status {
+    if (!ptr) return fail(GEMM_EPI_ERR_INVALID_VALUE, "%s is NULL", name);
+    if (ld < a->N) return fail(GEMM_EPI_ERR_INVALID_VALUE, "row stride of %s < N", name);
+    if (!aligned16(ptr) || ld % 8) return fail(GEMM_EPI_ERR_MISALIGNED, "%s: 16-byte base and stride needed", name);
+    return GEMM_EPI_OK;
+  };
+  auto vec = [&](const float* ptr, const char* name) -> gemm_epi_status {
+    if (!ptr) return fail(GEMM_EPI_ERR_INVALID_VALUE, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(ptr) & 3u) return fail(GEMM_EPI_ERR_MISALIGNED, "%s must be 4-byte aligned", name);
+    return GEMM_EPI_OK;
+  };
+  if (work) {
+    if ((s = tensor(a->dy, a->ld_dy, "dy")) || (s = tensor(a->x, a->ld_x, "x")) || (s = vec(a->s, "s"))) return s;
+    if (a->dx && ((s = tensor(a->dx, a->ld_dx, "dx")) || (s = vec(a->r, "r")))) return s;
+    if (a->dx && a->add && (s = tensor(a->add, a->ld_add, "add"))) return s;
+    if (a->w && (s = vec(a->w, "w"))) return s;
+  }
+  DeviceState* dev = nullptr;
+  if ((s = device_state(&dev, nullptr))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a->dw && a->N > 0) {
+    cudaError_t e = cudaMemsetAsync(a->dw, 0, sizeof(float) * a->N, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of dw");
+  }
+  if (!work) return GEMM_EPI_OK;
+  ge::RmsBwdParams p;
+  p.M = static_cast<int32_t>(a->M);
+  p.N = static_cast<int32_t>(a->N);
+  p.dy = static_cast<const uint16_t*>(a->dy);
+  p.ld_dy = a->ld_dy;
+  p.x = static_cast<const uint16_t*>(a->x);
+  p.ld_x = a->ld_x;
+  p.add = a->dx ? static_cast<const uint16_t*>(a->add) : nullptr;
+  p.ld_add = a->ld_add;
+  p.w = a->w;
+  p.s = a->s;
+  p.r = a->r;
+  p.dx = static_cast<uint16_t*>(a->dx);
+  p.ld_dx = a->ld_dx;
+  p.dw = a->dw;
+  // About 8 blocks of 256 threads per SM, striding over the rows.
+  const int64_t col_blocks = (a->N + ge::RB_COLS - 1) / ge::RB_COLS;
+  const int64_t want = std::max<int64_t>(1, 8LL * dev->sms / col_blocks);
+  const int64_t row_blocks = std::min<int64_t>(want, (a->M + ge::RB_TY - 1) / ge::RB_TY);
+  const dim3 grid(static_cast<unsigned>(col_blocks), static_cast<unsigned>(std::min<int64_t>(row_blocks, 65535)));
+  ge::rmsnorm_bwd_kernel<<<grid, dim3(ge::RB_TX, ge::RB_TY), 0, st>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the RMSNorm backward kernel");
 }
 
 gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void* workspace, void* stream) {

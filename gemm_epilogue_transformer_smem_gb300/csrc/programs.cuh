@@ -80,15 +80,4 @@ extern const int kNumSpecsFp8;
 // translation unit as kSpecsFp8.
 extern const void* const kDynamicFp8[2];
 
-struct SpecTable {
-  const KernelSpec* specs;
-  const int* n;
-};
-constexpr int kNumSpecTables = 3;
-inline const SpecTable* spec_tables() {
-  static const SpecTable t[kNumSpecTables] = {
-      {kSpecsForward, &kNumSpecsForward}, {kSpecsAux, &kNumSpecsAux}, {kSpecsFp8, &kNumSpecsFp8}};
-  return t;
-}
-
 }  // namespace ge

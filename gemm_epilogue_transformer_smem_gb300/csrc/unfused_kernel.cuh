@@ -32,6 +32,7 @@ struct UnfusedParams {
   const uint16_t* aux;  // residual or preact, row stride ld_aux
   int64_t ld_aux;
   const float* bias;
+  const float* col_scale;
   const float* row_scale;
   uint16_t* c;
   int64_t ldc;
@@ -59,6 +60,11 @@ __device__ __forceinline__ void uf_pointwise(const EpiOpDev& op, float (&v)[8], 
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (col0 + j < ncols) v[j] += __ldg(p.bias + col0 + j);
+      break;
+    case GEMM_EPI_OP_MUL_COL_SCALE:
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col0 + j < ncols) v[j] *= __ldg(p.col_scale + col0 + j);
       break;
     case GEMM_EPI_OP_MUL_ROW_SCALE:
 #pragma unroll
@@ -251,6 +257,11 @@ __global__ void __launch_bounds__(UF_THREADS)
           }
           break;
         }
+        case GEMM_EPI_OP_ROW_DOT:
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < valid) row_ss = fmaf(v[j], x[j], row_ss);
+          break;
         case GEMM_EPI_OP_ROW_RMS_RSQRT:
 #pragma unroll
           for (int j = 0; j < 8; ++j) {

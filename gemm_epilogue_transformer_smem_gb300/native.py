@@ -53,6 +53,8 @@ GEMM_EPI_OP_ROW_RMS_RSQRT = 13
 GEMM_EPI_OP_COL_SUM = 14
 GEMM_EPI_OP_PAIR_MUL = 15
 GEMM_EPI_OP_DSWIGLU = 16
+GEMM_EPI_OP_MUL_COL_SCALE = 17
+GEMM_EPI_OP_ROW_DOT = 18
 
 GEMM_EPI_MAX_OPS = 16
 GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1
@@ -93,6 +95,19 @@ class gemm_epi_args(ctypes.Structure):
         ("timeout_ms", ctypes.c_uint32), ("debug_flags", ctypes.c_uint32),
         ("B2", ctypes.c_void_p),
         ("a_scale_inv", ctypes.c_void_p), ("b_scale_inv", ctypes.c_void_p),
+        ("col_scale", ctypes.c_void_p),
+    ]
+
+
+class gemm_epi_rmsnorm_bwd_args(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+        ("dy", ctypes.c_void_p), ("ld_dy", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("ld_x", ctypes.c_int64),
+        ("add", ctypes.c_void_p), ("ld_add", ctypes.c_int64),
+        ("w", ctypes.c_void_p), ("s", ctypes.c_void_p), ("r", ctypes.c_void_p),
+        ("dx", ctypes.c_void_p), ("ld_dx", ctypes.c_int64),
+        ("dw", ctypes.c_void_p),
     ]
 
 
@@ -108,6 +123,7 @@ SIGNATURES = [
     ("gemm_epi_run_unfused", ctypes.c_int,
      [gemm_epi_handle, ctypes.POINTER(gemm_epi_args), ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     ("gemm_epi_run_no_alloc", ctypes.c_int, [gemm_epi_handle, ctypes.POINTER(gemm_epi_args), ctypes.c_void_p]),
+    ("gemm_epi_rmsnorm_backward", ctypes.c_int, [ctypes.POINTER(gemm_epi_rmsnorm_bwd_args), ctypes.c_void_p]),
     ("gemm_epi_query_status", ctypes.c_int, [gemm_epi_handle, ctypes.c_void_p, ctypes.c_void_p]),
     ("gemm_epi_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("gemm_epi_last_error", ctypes.c_char_p, []),

@@ -28,6 +28,13 @@ them; "N(0, s)" has standard deviation s):
             14336x4096 (N x K) N(0, 0.02); preact (the forward gate / up pairs,
             interleaved) 8192x28672 N(0, 1.28), the spread of the swiglu
             workload's own GEMM output (0.02 * sqrt(4096)); out 8192x28672.
+  drmsnorm  the RMSNorm backward at the down-projection's output: dy = dH @ W
+            (dH 16384x14336 N(0,1), W 14336x4096 N(0, 0.02)) is stored, scaled
+            by the norm weight w (fp32 N(1, 0.1)) and reduced against the
+            RMSNorm input x (the residual stream, 16384x4096 N(0,1)) per row;
+            a second pass (gemm_epi_rmsnorm_backward) gives dx and dw from it
+            and the forward's S (fp32, 1 + N(0, 0.05), what the forward's row
+            statistic holds for rows of unit mean square).
   fp8in     the fp8 workload's program on FP8 operands: the next layer of the
             FP8 loop reads the e4m3 activations the fp8 workload emits.
             M = N = K = 8192.  A: e4m3 codes of max(N(0, 0.1), 0) * 112 (the
@@ -36,7 +43,7 @@ them; "N(0, s)" has standard deviation s):
             N(0,1)/sqrt(K), as e4m3 codes at scale 112 * sqrt(K) (448/4 of its
             own standard deviation), dequantised by the reciprocal.
 
-Draw order per workload: A, B, bias, residual / preact, B2.  Each tensor is drawn
+Draw order per workload: A, B, bias, residual / preact, B2, column scale, S.  Each tensor is drawn
 in fp32 with ``torch.randn`` from one generator seeded with 1000 + index,
 scaled, then cast to bf16 (round to nearest even); bias stays fp32.  FP8
 operands are multiplied by their quantisation scale, clamped to the format's
@@ -73,6 +80,8 @@ class Workload:
     a_relu: bool = False    # A drawn as max(N(0, a_std), 0)
     a_qscale: float = 1.0   # FP8 quantisation scales of A and B
     b_qscale: float = 1.0
+    col_scale_std: Optional[float] = None   # column scale drawn as 1 + N(0, std)
+    finish: Optional[str] = None            # a second pass after the GEMM ("rmsnorm_backward")
     notes: str = ""
 
     @property
@@ -122,6 +131,9 @@ WORKLOADS = {
                          a_std=1.0, b_std=0.02, aux="preact"),
     "dswiglu": Workload("dswiglu", 7, 8192, 14336, 4096, "nk", ("dswiglu", "store_bf16"),
                         a_std=1.0, b_std=0.02, aux="preact", aux_std=1.28),
+    "drmsnorm": Workload("drmsnorm", 8, 16384, 4096, 14336, "kn", ("store_bf16", "col_scale", "row_dot"),
+                         a_std=1.0, b_std=0.02, aux="residual", col_scale_std=0.1,
+                         finish="rmsnorm_backward"),
     "fp8in": Workload("fp8in", 6, 8192, 8192, 8192, "nk",
                       ("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"),
                       a_std=0.1, b_std=1 / math.sqrt(8192), bias_std=0.1, alpha=0.5,
@@ -143,6 +155,8 @@ class Inputs:
     B2: Optional[torch.Tensor] = None  # second weight operand, B's shape
     a_scale_inv: Optional[torch.Tensor] = None  # FP8 dequantisation factors, 1 fp32 each
     b_scale_inv: Optional[torch.Tensor] = None
+    col_scale: Optional[torch.Tensor] = None    # fp32, one per output column
+    row_stat: Optional[torch.Tensor] = None     # fp32, one per row (the forward's S)
     extra: dict = field(default_factory=dict)
 
 
@@ -184,6 +198,10 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs
     aux = draw((w.M, w.n_out), w.aux_std) if w.aux else None
     B2 = operand(tuple(B.shape), w.b_std, w.b_qscale) if w.dual else None
     inp = Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale, B2=B2)
+    if w.col_scale_std is not None:
+        inp.col_scale = 1.0 + draw((w.n_out,), w.col_scale_std, torch.float32)
+    if w.finish == "rmsnorm_backward":
+        inp.row_stat = 1.0 + draw((w.M,), 0.05, torch.float32)
     if w.in_type != "bf16":
         inp.a_scale_inv = torch.tensor([1.0 / w.a_qscale], dtype=torch.float32, device=device)
         inp.b_scale_inv = torch.tensor([1.0 / w.b_qscale], dtype=torch.float32, device=device)

@@ -26,7 +26,9 @@
  *  - SwiGLU out = up * silu(gate): Superoptimizer, section 7 "SwiGLU"; the
  *    RMSNorm-MLP's out = up * gate on rows scaled by S: section 10.
  *  - RMSNorm S = 1/sqrt(mean(x^2) + eps) and the row-broadcast rewrite
- *    (X*S)@W = (X@W)*S: Superoptimizer, sections 3 and 9 "RMSNorm".
+ *    (X*S)@W = (X@W)*S: Superoptimizer, sections 3 and 9 "RMSNorm"; its
+ *    backward as a row reduction on the output tile plus a second pass
+ *    (ROW_DOT, gemm_epi_rmsnorm_backward; CODA's backward epilogues).
  *  - a small set of composable epilogue primitives (scaling, reductions,
  *    pairwise transforms, accumulation) finished on the on-chip output tile,
  *    covering forward and backward work: "CODA: ... GEMM-Epilogue"
@@ -94,6 +96,14 @@ extern "C" {
 
 #define GEMM_EPI_VERSION 1
 
+/* The library is built with hidden symbol visibility: only these entry
+ * points are exported, so several copies of it can share one process. */
+#if defined(__GNUC__)
+#define GEMM_EPI_API __attribute__((visibility("default")))
+#else
+#define GEMM_EPI_API
+#endif
+
 typedef enum gemm_epi_status {
     GEMM_EPI_OK = 0,
     GEMM_EPI_ERR_INVALID_VALUE = 1, /* bad size, NULL where required, bad program */
@@ -152,7 +162,7 @@ typedef enum gemm_epi_op_code {
     GEMM_EPI_OP_PAIR_MUL = 15,          /* y'[m,j] = y[m,gate(j)] * y[m,up(j)]: the RMSNorm-MLP's
                                            plain up * gate; same groups and N_out as
                                            PAIR_SWIGLU, at most one pair op per program      */
-    GEMM_EPI_OP_DSWIGLU = 16            /* backward of PAIR_SWIGLU: y[m,j] = dh for
+    GEMM_EPI_OP_DSWIGLU = 16,           /* backward of PAIR_SWIGLU: y[m,j] = dh for
                                            h = silu(gate) * up; gate = preact[m, gate(j)],
                                            up = preact[m, up(j)] (args.preact, the forward
                                            pre-activations, M x 2N); writes
@@ -165,6 +175,12 @@ typedef enum gemm_epi_op_code {
                                            columns, ops after it the 2N outputs; no other
                                            op may read preact or residual.  Counts as the
                                            program's pair op.                               */
+    GEMM_EPI_OP_MUL_COL_SCALE = 17,     /* y = y * col_scale[n]     (args.col_scale)        */
+    GEMM_EPI_OP_ROW_DOT = 18            /* row_out[m] = sum over n of y * residual[m, n]
+                                           (args.residual): the row reduction of the
+                                           RMSNorm backward, finished by
+                                           gemm_epi_rmsnorm_backward.  Not with
+                                           ROW_RMS_RSQRT (both write row_out).              */
 } gemm_epi_op_code;
 
 typedef struct gemm_epi_op {
@@ -223,6 +239,7 @@ typedef struct gemm_epi_args {
      * the next GEMM without a host round trip.  Any operand type. */
     const float *a_scale_inv;
     const float *b_scale_inv;
+    const float *col_scale;   /* MUL_COL_SCALE: fp32, one value per column at its point of use */
 } gemm_epi_args;
 
 /* Test hook: the producer skips the first operand load of the first CTA so
@@ -241,28 +258,28 @@ typedef struct gemm_epi_plan *gemm_epi_handle;
 
 /* Validates the descriptor and builds a host-side plan.  Pure host code: no
  * CUDA call, no device needed.  *out is set only on GEMM_EPI_OK. */
-gemm_epi_status gemm_epi_create(gemm_epi_handle *out, const gemm_epi_desc *desc);
+GEMM_EPI_API gemm_epi_status gemm_epi_create(gemm_epi_handle *out, const gemm_epi_desc *desc);
 
 /* Frees the plan.  NULL is accepted. */
-gemm_epi_status gemm_epi_destroy(gemm_epi_handle h);
+GEMM_EPI_API gemm_epi_status gemm_epi_destroy(gemm_epi_handle h);
 
 /* Bytes of device workspace gemm_epi_run needs for this plan (>= 256). */
-size_t gemm_epi_workspace_size(gemm_epi_handle h);
+GEMM_EPI_API size_t gemm_epi_workspace_size(gemm_epi_handle h);
 
 /* Output columns of the plan (N, N/2 after a pair op, 2N after DSWIGLU); -1 for NULL. */
-int64_t gemm_epi_out_cols(gemm_epi_handle h);
+GEMM_EPI_API int64_t gemm_epi_out_cols(gemm_epi_handle h);
 
 /* Enqueues the fused kernel on `stream`.  Checks the device (compute
  * capability 10.x), every pointer the program uses (non-NULL, 16-byte
  * aligned) and the workspace.  Asynchronous; capture-safe. */
-gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
+GEMM_EPI_API gemm_epi_status gemm_epi_run(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
 
 /* The unfused baseline with the same semantics: a bare GEMM into `scratch`
  * (M x N bf16 pre-epilogue accumulator, row stride ld_scratch >= N, caller
  * owned), then a separate memory-bound epilogue pass that reads it back.  The
  * accumulator is rounded to bf16 between the two, so results differ from the
  * fused path by that rounding.  For measurement only. */
-gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args *args,
+GEMM_EPI_API gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args *args,
                                      void *scratch, int64_t ld_scratch, void *stream);
 
 /* Allocation-free variant of gemm_epi_run.  The pages have no counterpart:
@@ -288,20 +305,49 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args *arg
  *    reported back; use gemm_epi_run with a workspace and
  *    gemm_epi_query_status when the status is needed. */
 #define GEMM_EPI_NO_ALLOC_SCRATCH_BYTES 65536
-gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
+GEMM_EPI_API gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
 
 /* Synchronises `stream`, then reads the status word the last run on that
  * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
-gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
+/*
+ * RMSNorm backward, second pass.  For y = x * S * w (S[m] = 1/sqrt(mean_n
+ * x^2 + eps), the forward's ROW_RMS_RSQRT output) and the upstream gradient
+ * dy (the C of a GEMM whose program ran MUL_COL_SCALE(w) and ROW_DOT with
+ * residual = x after storing dy):
+ *   dx[m,n] = S[m] w[n] dy[m,n] - x[m,n] S[m]^3 r[m] / N  (+ add[m,n])
+ *   dw[n]   = sum over m of dy[m,n] x[m,n] S[m]
+ * with r = the ROW_DOT output.  The per-row reduction spans every column of
+ * the row, so this step follows the GEMM as its own memory-bound kernel
+ * (reads dy, x and add once, writes dx once).  dy, x, add, dx: bf16 row-major,
+ * 16-byte aligned, row strides multiples of 8 elements.  w NULL means 1; add
+ * NULL means none; dx or dw may be NULL (not computed); dw is overwritten.
+ */
+typedef struct gemm_epi_rmsnorm_bwd_args {
+    int64_t M, N;
+    const void *dy;  int64_t ld_dy;
+    const void *x;   int64_t ld_x;
+    const void *add; int64_t ld_add;
+    const float *w;  /* N values */
+    const float *s;  /* M values */
+    const float *r;  /* M values */
+    void *dx;        int64_t ld_dx;
+    float *dw;       /* N values */
+} gemm_epi_rmsnorm_bwd_args;
+
+/* Enqueues the second pass on `stream` (a cudaStream_t).  Asynchronous;
+ * capture-safe; checks sizes, pointers and alignment first. */
+GEMM_EPI_API gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bwd_args *args, void *stream);
+
+GEMM_EPI_API gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
 
 /* Static description of a status code. */
-const char *gemm_epi_status_string(gemm_epi_status s);
+GEMM_EPI_API const char *gemm_epi_status_string(gemm_epi_status s);
 
 /* One-line reason for the most recent failure on this thread ("" if none). */
-const char *gemm_epi_last_error(void);
+GEMM_EPI_API const char *gemm_epi_last_error(void);
 
 /* GEMM_EPI_VERSION of the loaded library. */
-int gemm_epi_version(void);
+GEMM_EPI_API int gemm_epi_version(void);
 
 #ifdef __cplusplus
 }

@@ -113,7 +113,8 @@ def oracle_problem(w: synth.Workload, inp: synth.Inputs) -> oracle.Problem:
         residual=aux if w.aux == "residual" else None,
         preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
         B2=operand_host(inp.B2, w.in_type), a_type=w.in_type, b_type=w.in_type,
-        a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv))
+        a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv),
+        col_scale=None if inp.col_scale is None else inp.col_scale.detach().cpu().numpy())
 
 
 def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
@@ -125,7 +126,7 @@ def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
         scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=inp.A.device)
     api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
                     bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, B2=inp.B2,
-                    a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv, **kw)
+                    a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv, col_scale=inp.col_scale, **kw)
     torch.cuda.synchronize()
     status = plan.query_status(out.workspace)
     assert status == 0, "kernel status %d" % status
@@ -143,11 +144,32 @@ def compare_rows(w, inp, out, rows=None, oracle_p=None):
         check_bf16(bits(out.C[sel]), ref["y"], "C")
     if out.C8 is not None:
         check_e4m3(out.C8[sel].cpu().numpy(), ref["c_e4m3"], ref["y"] * inp.fp8_scale)
-    if out.row_out is not None:
+    if out.row_out is not None and "row_dot" in prog:
+        # sum_n y x can cancel: bound by the sum of the magnitudes of its terms
+        check_cols(out.row_out[sel].cpu().numpy(), ref["row_stat"], row_dot_abs(w, inp, ref, rows))
+    elif out.row_out is not None:
         check_rows(out.row_out[sel].cpu().numpy(), ref["row_stat"])
     if "amax" in prog and rows is None:
         check_amax(float(out.amax.item()), ref["amax"])
     return ref
+
+
+def row_dot_abs(w, inp, ref, rows):
+    """sum_n |w[n] y[m,n] x[m,n]| for the row_dot of the drmsnorm program
+    (store_bf16, col_scale, row_dot), from the oracle's stored values."""
+    x = oracle.bf16_bits_to_f64(bits(inp.aux if rows is None else inp.aux[torch.as_tensor(np.asarray(rows))]))
+    cs = inp.col_scale.detach().cpu().numpy().astype(np.float64)
+    return np.abs(ref["y"] * cs[None, :] * x).sum(1)
+
+
+def run_finish(w, inp, out):
+    """The workload's second pass (gemm_epi_rmsnorm_backward) on the GEMM's
+    outputs: returns (dx, dw) device tensors."""
+    dx = torch.empty(out.C.shape, dtype=torch.bfloat16, device=out.C.device)
+    dw = torch.empty(out.C.shape[1], dtype=torch.float32, device=out.C.device)
+    api.rmsnorm_backward(out.C, inp.aux, inp.row_stat, out.row_out, w=inp.col_scale, dx=dx, dw=dw)
+    torch.cuda.synchronize()
+    return dx, dw
 
 
 def compare_cols(w, inp, out, cols, oracle_p=None):

@@ -39,6 +39,17 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == {s[0] for s in N.SIGNATURES}
 
 
+def test_only_the_c_abi_is_exported(lib):
+    """Hidden visibility: the library exports exactly the declared entry
+    points and no GNU-unique symbols, which the loader would otherwise merge
+    across two copies of the library in one process."""
+    out = subprocess.run(["nm", "-D", "--defined-only", N.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    defined = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert defined == set(declared_functions()), sorted(defined ^ set(declared_functions()))
+    assert not any(line.split()[1] == "u" for line in out.splitlines() if len(line.split()) >= 3)
+
+
 def test_struct_layouts_match_header(lib, tmp_path):
     """Size and every field offset of the three structs, as a C compiler lays
     them out from the header, against the ctypes binding."""
@@ -254,3 +265,36 @@ def test_create_checks_batch_strides(lib):
                 dict(batch_stride_aux=256 * 512 - 8), dict(batch=-1), dict(batch=70000)):
         s, h, _ = desc(**bad)
         assert s == N.GEMM_EPI_ERR_INVALID_VALUE, bad
+
+
+@pytest.mark.parametrize("name", sorted(__import__("gemm_epilogue_transformer_smem_gb300.synth",
+                                                   fromlist=["WORKLOADS"]).WORKLOADS))
+def test_binding_supplies_every_argument_a_workload_needs(lib, name):
+    """Each workload's program through the Python binding with host tensors:
+    every pointer the program uses is present and aligned, so the call gets
+    past the argument checks and stops only at the missing GPU."""
+    import torch
+    from gemm_epilogue_transformer_smem_gb300 import synth
+    w = synth.WORKLOADS[name]
+    w = w.scaled(min(w.M, 96), min(w.N, 512), min(w.K, 128))
+    inp = synth.make_inputs(w, "cpu")
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, a_type=w.in_type,
+                    b_type=w.in_type)
+    out = api.allocate_outputs(plan, "cpu")
+    with pytest.raises(N.GemmEpiError) as err:
+        api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias,
+                        aux=inp.aux, B2=inp.B2, a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv,
+                        col_scale=inp.col_scale, stream=FakeStream())
+    assert err.value.status in (N.GEMM_EPI_ERR_CUDA, N.GEMM_EPI_ERR_ARCH), str(err.value)
+    if w.finish == "rmsnorm_backward":
+        dx = torch.empty(out.C.shape, dtype=torch.bfloat16)
+        dw = torch.empty(out.C.shape[1])
+        with pytest.raises(N.GemmEpiError) as err:
+            api.rmsnorm_backward(out.C, inp.aux, inp.row_stat, out.row_out, w=inp.col_scale, dx=dx, dw=dw,
+                                 stream=FakeStream())
+        assert err.value.status in (N.GEMM_EPI_ERR_CUDA, N.GEMM_EPI_ERR_ARCH), str(err.value)
+
+
+class FakeStream:
+    """Stands in for a torch CUDA stream on a machine without a GPU."""
+    cuda_stream = 0

@@ -44,6 +44,7 @@ SMALL_SHAPES = [
     ("swiglu2w", 300, 768, 200),    # separate gate / up weights, 384 output columns
     ("fp8in", 257, 528, 272),       # e4m3 operands, K tail of 16 (one 16-byte group)
     ("dswiglu", 300, 520, 200),     # SwiGLU backward: 1040 output columns, 8-column N tail
+    ("drmsnorm", 300, 1000, 200),   # dy stored, column scale, row dot with x
 ]
 
 
@@ -364,7 +365,7 @@ def test_graph_capture_replay_matches_eager():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu"]
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu", "drmsnorm"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -423,3 +424,31 @@ def test_dswiglu_groups_and_ops(g, layout, variant):
     check_amax(float(out.amax.item()), r["amax"])
     c = p.cols(list(range(2 * N)))
     check_cols(out.col_out.cpu().numpy(), c["col_stat"], np.abs(c["y"]).sum(0))
+
+
+def test_two_library_copies_in_one_process(tmp_path):
+    """A second copy of the library, loaded beside the first, launches its
+    own kernels (each copy keeps its own kernel tables)."""
+    import shutil
+    copy = str(tmp_path / "libgemm_epi_copy.so")
+    shutil.copy(native.LIB_PATH, copy)
+    first = native.load()
+    M, N, K = 200, 264, 128
+    gen = torch.Generator(device=DEV).manual_seed(80)
+    A = torch.randn(M, K, generator=gen, device=DEV).to(torch.bfloat16)
+    B = torch.randn(K, N, generator=gen, device=DEV).to(torch.bfloat16)
+    ref = oracle.Problem(bits(A), bits(B), ["gelu_tanh", "store_bf16"]).rows()["y"]
+    results = []
+    try:
+        for lib_path in (native.LIB_PATH, copy, native.LIB_PATH):
+            native._lib = first if lib_path == native.LIB_PATH else native.load(copy)
+            plan = api.Plan(M, N, K, ["gelu_tanh", "store_bf16"])
+            out = api.allocate_outputs(plan, DEV)
+            api.run_program(plan, A, B, out)
+            torch.cuda.synchronize()
+            assert plan.query_status(out.workspace) == 0
+            results.append(bits(out.C))
+    finally:
+        native._lib = first
+    for r in results:
+        check_bf16(r, ref)
