@@ -39,6 +39,9 @@ using ProgResidualRms = StaticProgram<GEMM_EPI_OP_ADD_RESIDUAL, GEMM_EPI_OP_STOR
 // SwiGLU backward: both gradients from dh and the forward gate / up pairs.
 constexpr int DSWIGLU_G1 = GEMM_EPI_OP_DSWIGLU | (1 << 8);
 using ProgDSwiGLU = StaticProgram<DSWIGLU_G1, GEMM_EPI_OP_STORE_BF16>;
+// RMSNorm backward, first pass: store dy, scale by the norm weight, reduce
+// against the RMSNorm input per row.
+using ProgRmsBwd = StaticProgram<GEMM_EPI_OP_STORE_BF16, GEMM_EPI_OP_MUL_COL_SCALE, GEMM_EPI_OP_ROW_DOT>;
 // acc * gelu_tanh'(preact), bf16 store, column sums.
 using ProgGeluGradColSum = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16,
                                          GEMM_EPI_OP_COL_SUM>;

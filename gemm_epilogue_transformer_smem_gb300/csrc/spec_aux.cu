@@ -1,6 +1,6 @@
-// spec_aux.cu -- static kernels of the FP8, residual + row RMS, GELU backward
-// and SwiGLU backward programs (compiled apart from the others to keep builds
-// parallel).
+// spec_aux.cu -- static kernels of the FP8, residual + row RMS, GELU backward,
+// SwiGLU backward and RMSNorm backward programs (compiled apart from the
+// others to keep builds parallel).
 #include "programs.cuh"
 
 namespace ge {
@@ -10,6 +10,7 @@ const KernelSpec kSpecsAux[] = {
     make_spec<ProgResidualRms>("residual_row_rms"),
     make_spec<ProgGeluGradColSum>("gelu_grad_col_sum"),
     make_spec<ProgDSwiGLU>("dswiglu"),
+    make_spec<ProgRmsBwd>("rmsnorm_backward_dy"),
 };
 const int kNumSpecsAux = sizeof(kSpecsAux) / sizeof(kSpecsAux[0]);
 
