@@ -24,6 +24,8 @@ PROGRAMS = {
     "fp8": (("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"), "kn"),
     "residual_rms": (("residual", "store_bf16", "row_rms:1e-6"), "nk"),
     "grad_colsum": (("row_scale", "gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
+    "dswiglu": (("alpha", "dswiglu", "store_bf16", "amax"), "nk"),
+    "rms_bwd": (("store_bf16", "col_scale", "row_dot"), "kn"),
 }
 
 
@@ -47,30 +49,37 @@ def test_batched_matches_per_batch_oracle(name, shared_b, variant):
     A = rnd(Bt, M, K)
     bshape = (K, N) if layout == "kn" else (N, K)
     B = rnd(*bshape) if shared_b else rnd(Bt, *bshape)
+    n_out = api.out_cols(list(program), N)
     bias = torch.randn(N, generator=g, device=DEV) * 0.1
-    aux = rnd(Bt, M, N, std=1.0)
+    aux = rnd(Bt, M, n_out, std=1.0)
     row_scale = torch.rand(Bt, M, generator=g, device=DEV) + 0.5
+    col_scale = torch.rand(n_out, generator=g, device=DEV) + 0.5
     plan = api.Plan(M, N, K, program, b_layout=layout, batch=Bt, batch_stride_b=0 if shared_b else None)
     out = api.allocate_outputs(plan, DEV)
     api.run_program(plan, A, B, out, alpha=0.75, fp8_scale=64.0, bias=bias, row_scale=row_scale, aux=aux,
-                    debug_flags=VARIANTS[variant])
+                    col_scale=col_scale, debug_flags=VARIANTS[variant])
     torch.cuda.synchronize()
     assert plan.query_status(out.workspace) == 0
 
     amax = 0.0
     for b in range(Bt):
+        names = [op.partition(":")[0] for op in program]
         p = oracle.Problem(bits(A[b]), bits(B if shared_b else B[b]), list(program), b_is_nk=(layout == "nk"),
                            alpha=0.75, bias=bias.cpu().numpy(), row_scale=row_scale[b].cpu().numpy(),
-                           residual=bits(aux[b]) if "residual" in program else None,
-                           preact=bits(aux[b]) if "gelu_tanh_grad" in program else None, fp8_scale=64.0)
+                           residual=bits(aux[b]) if any(n in api.RESIDUAL_OPS for n in names) else None,
+                           preact=bits(aux[b]) if any(n in api.PREACT_OPS for n in names) else None, fp8_scale=64.0,
+                           col_scale=col_scale.cpu().numpy())
         r = p.rows()
         check_bf16(bits(out.C[b]), r["y"], "C[%d]" % b)
         if out.C8 is not None:
             check_e4m3(out.C8[b].cpu().numpy(), r["c_e4m3"], r["y"] * 64.0)
-        if out.row_out is not None:
+        if out.row_out is not None and "row_dot" in names:
+            terms = r["y"] * col_scale.double().cpu().numpy()[None, :] * oracle.bf16_bits_to_f64(bits(aux[b]))
+            check_cols(out.row_out[b].cpu().numpy(), r["row_stat"], np.abs(terms).sum(1))
+        elif out.row_out is not None:
             check_rows(out.row_out[b].cpu().numpy(), r["row_stat"])
         if out.col_out is not None:
-            cs = p.cols(list(range(N)))
+            cs = p.cols(list(range(n_out)))
             check_cols(out.col_out[b].cpu().numpy(), cs["col_stat"], np.abs(cs["y"]).sum(0))
         amax = max(amax, r["amax"])
     if out.amax is not None:

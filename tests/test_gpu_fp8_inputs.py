@@ -188,3 +188,26 @@ def test_fp8_loop_chain():
     bound = 2e-2 * np.maximum(np.abs(r2["y"]), 1e-2 * rms) + prop
     bad = np.abs(g2 - r2["y"]) > bound
     assert not bad.any(), "chain output: %d of %d outside the propagated bound" % (int(bad.sum()), bad.size)
+
+
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+def test_fp8_backward_program(variant):
+    """A backward GEMM of the FP8 loop: e5m2 gradients times e4m3 weights,
+    finished by the SwiGLU backward epilogue."""
+    M, N, K = 260, 272, 192
+    g = torch.Generator(device=DEV).manual_seed(37)
+    A = codes((M, K), "e5m2", 64.0, g)
+    B = codes((N, K), "e4m3", 64.0, g)
+    pre = (torch.randn(M, 2 * N, generator=g, device=DEV) * 1.3).to(torch.bfloat16)
+    sa, sb = 1.0 / 64.0, 1.0 / (64.0 * K ** 0.5)
+    prog = ["dswiglu", "amax", "store_bf16"]
+    plan = api.Plan(M, N, K, prog, b_layout="nk", a_type="e5m2", b_type="e4m3")
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out, aux=pre, a_scale_inv=dev_scalar(sa), b_scale_inv=dev_scalar(sb),
+                    debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    r = oracle.Problem(host(A), host(B), prog, b_is_nk=True, preact=bits(pre), a_type="e5m2", b_type="e4m3",
+                       a_scale_inv=sa, b_scale_inv=sb).rows()
+    check_bf16(bits(out.C), r["y"])
+    check_amax(float(out.amax.item()), r["amax"])
