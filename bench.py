@@ -485,45 +485,109 @@ def time_steps_split(first, second, steps, stream):
 
 
 def measure_e2e(plan, w, inp, out, kw, dev, steps, world, fin=None):
-    """Same metric through the C ABI with host buffers: every step copies the
-    inputs from pinned host memory, runs, and reads the outputs back."""
+    """Same metric through the C ABI with host buffers: every step copies its
+    inputs from pinned host memory, runs, and reads its outputs back.
+
+    Pipelined (the reported value): step i's host-to-device copy, compute and
+    device-to-host copy run on three streams over two device buffer sets, so
+    one step's transfers overlap its neighbours' kernels; events guard each
+    buffer's reuse.  The serial figure (copy in, run, copy out, one stream)
+    is reported beside it."""
     import torch
     from gemm_epilogue_transformer_smem_gb300 import api
 
-    h = {k: (v.cpu().pin_memory() if v is not None else None)
-         for k, v in (("A", inp.A), ("B", inp.B), ("bias", inp.bias), ("aux", inp.aux), ("B2", inp.B2),
-                      ("a_scale_inv", inp.a_scale_inv), ("b_scale_inv", inp.b_scale_inv),
-                      ("col_scale", inp.col_scale), ("row_stat", inp.row_stat))}
-    d = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
-    outs = [t for t in (out.C, out.C8, out.amax, out.row_out, out.col_out) if t is not None]
-    if fin:
-        outs += list(fin.outputs)
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
-    stream = torch.cuda.current_stream(dev)
+    names = ("A", "B", "bias", "aux", "B2", "a_scale_inv", "b_scale_inv", "col_scale", "row_stat")
+    src = dict(zip(names, (inp.A, inp.B, inp.bias, inp.aux, inp.B2, inp.a_scale_inv, inp.b_scale_inv,
+                           inp.col_scale, inp.row_stat)))
+    h = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in src.items()}
 
-    def step():
+    def buffers():
+        d = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
+        o = api.allocate_outputs(plan, dev)
+        f = make_finish(w, inp, o, dev) if fin else None
+        outs = [t for t in (o.C, o.C8, o.amax, o.row_out, o.col_out) if t is not None]
+        if f:
+            outs += list(f.outputs)
+        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        return {"d": d, "o": o, "f": f, "outs": outs, "ho": ho}
+
+    sets = [buffers(), buffers()]
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0]["outs"])
+
+    def copy_in(b):
         for k, v in h.items():
             if v is not None:
-                d[k].copy_(v, non_blocking=True)
-        api.run_program(plan, d["A"], d["B"], out, alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
+                b["d"][k].copy_(v, non_blocking=True)
+
+    def compute(b, stream=None):
+        d = b["d"]
+        api.run_program(plan, d["A"], d["B"], b["o"], alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
                         bias=d["bias"], aux=d["aux"], B2=d["B2"], a_scale_inv=d["a_scale_inv"],
-                        b_scale_inv=d["b_scale_inv"], col_scale=d["col_scale"])
-        if fin:
-            fin(aux=d["aux"], w_=d["col_scale"], s_=d["row_stat"])
-        for t, ht in zip(outs, host_out):
+                        b_scale_inv=d["b_scale_inv"], col_scale=d["col_scale"], stream=stream)
+        if b["f"]:
+            b["f"](aux=d["aux"], w_=d["col_scale"], s_=d["row_stat"])
+
+    def copy_out(b):
+        for t, ht in zip(b["outs"], b["ho"]):
             ht.copy_(t, non_blocking=True)
 
+    # Serial: one stream, one buffer set.
+    stream = torch.cuda.current_stream(dev)
+
+    def serial_step():
+        copy_in(sets[0])
+        compute(sets[0])
+        copy_out(sets[0])
+
     for _ in range(2):
-        step()
+        serial_step()
     torch.cuda.synchronize()
     barrier(world)
-    seconds = time_steps(step, steps, stream)
-    seconds = max_over_ranks(seconds, world)
+    serial_s = max_over_ranks(time_steps(serial_step, steps, stream), world)
+
+    # Pipelined: three streams, two buffer sets.
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, run_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def pipelined(n):
+        for i in range(n):
+            k = i % 2
+            b = sets[k]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(run_done[k])      # step i-2's kernel has read these inputs
+                copy_in(b)
+                in_ready[k].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(in_ready[k])
+                if i >= 2:
+                    s_run.wait_event(out_done[k])     # step i-2's outputs have been read back
+                compute(b, stream=s_run)
+                run_done[k].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(run_done[k])
+                copy_out(b)
+                out_done[k].record(s_out)
+
+    pipelined(4)
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    pipelined(steps)
+    s_in.wait_stream(s_out)
+    end.record(s_in)
+    end.synchronize()
+    seconds = max_over_ranks(start.elapsed_time(end) / 1e3, world)
     value = aggregate_value(float(w.flops) * steps, world, seconds) / 1e12
     return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": seconds / steps * 1e3}
+            "ms_per_step": seconds / steps * 1e3,
+            "mode": "pipelined: copy-in, compute and copy-out of consecutive steps on three streams, "
+                    "two device buffer sets",
+            "serial_value": aggregate_value(float(w.flops) * steps, world, serial_s) / 1e12,
+            "serial_ms_per_step": serial_s / steps * 1e3}
 
 
 def main():
