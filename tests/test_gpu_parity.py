@@ -452,3 +452,61 @@ def test_two_library_copies_in_one_process(tmp_path):
         native._lib = first
     for r in results:
         check_bf16(r, ref)
+
+
+# ------------------------------------------------------------ edge cases of the wider ops
+
+@pytest.mark.parametrize("variant", ["1sm", "interp"])
+def test_zero_k_backward_ops(variant):
+    """K == 0: the accumulator is zero, so DSWIGLU gives the post-op bias
+    alone and ROW_DOT gives zero sums, without reading A or B."""
+    M, N = 130, 272
+    gen = torch.Generator(device=DEV).manual_seed(90)
+    A = torch.empty(M, 0, dtype=torch.bfloat16, device=DEV)
+    B = torch.empty(0, N, dtype=torch.bfloat16, device=DEV)
+    pre = torch.randn(M, 2 * N, generator=gen, device=DEV).to(torch.bfloat16)
+    bias = torch.randn(2 * N, generator=gen, device=DEV)
+    plan = api.Plan(M, N, 0, ["dswiglu", "bias", "store_bf16"])
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out, aux=pre, bias=bias, debug_flags=VARIANTS[variant])
+    x = torch.randn(M, N, generator=gen, device=DEV).to(torch.bfloat16)
+    cs = torch.rand(N, generator=gen, device=DEV) + 0.5
+    plan2 = api.Plan(M, N, 0, ["store_bf16", "col_scale", "row_dot"])
+    out2 = api.allocate_outputs(plan2, DEV)
+    out2.row_out.fill_(5.0)
+    api.run_program(plan2, A, B, out2, aux=x, col_scale=cs, debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0 and plan2.query_status(out2.workspace) == 0
+    check_bf16(bits(out.C), np.broadcast_to(bias.cpu().numpy().astype(np.float64), (M, 2 * N)))
+    assert torch.all(out2.C.float() == 0) and torch.all(out2.row_out == 0)
+
+
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+def test_batched_two_weight_swiglu(variant):
+    """Batches with separate gate / up weights (B and B2 advance together)."""
+    Bt, M, N, K = 2, 200, 512, 136
+    gen = torch.Generator(device=DEV).manual_seed(91)
+    A = (torch.randn(Bt, M, K, generator=gen, device=DEV) * 0.5).to(torch.bfloat16)
+    B = (torch.randn(Bt, K, N // 2, generator=gen, device=DEV) * 0.1).to(torch.bfloat16)
+    B2 = (torch.randn(Bt, K, N // 2, generator=gen, device=DEV) * 0.1).to(torch.bfloat16)
+    prog = ["pair_swiglu:128", "store_bf16"]
+    plan = api.Plan(M, N, K, prog, dual=True, batch=Bt)
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out, B2=B2, debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    for b in range(Bt):
+        r = oracle.Problem(bits(A[b]), bits(B[b]), prog, B2=bits(B2[b])).rows()
+        check_bf16(bits(out.C[b]), r["y"], "C[%d]" % b)
+
+
+def test_rmsnorm_backward_empty_shapes():
+    """M == 0 or N == 0 launches nothing; dw is still overwritten with zeros."""
+    dw = torch.full((16,), 3.0, device=DEV)
+    empty = torch.empty(0, 16, dtype=torch.bfloat16, device=DEV)
+    s = torch.empty(0, device=DEV)
+    api.rmsnorm_backward(empty, empty, s, s, dx=empty, dw=dw)
+    none = torch.empty(4, 0, dtype=torch.bfloat16, device=DEV)
+    api.rmsnorm_backward(none, none, torch.ones(4, device=DEV), torch.ones(4, device=DEV), dx=none)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0)
