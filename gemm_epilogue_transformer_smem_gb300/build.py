@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_epi.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["gemm_epi.cu", "spec_forward.cu", "spec_aux.cu", "spec_fp8.cu"]
+UNITS = ["gemm_epi.cu", "spec_forward.cu", "spec_aux.cu", "spec_fp8.cu", "spec_common.cu"]
 
 
 def sources(csrc=CSRC):

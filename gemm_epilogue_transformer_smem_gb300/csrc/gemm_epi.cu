@@ -66,7 +66,8 @@ struct SpecTable {
   const int* n;
 };
 const SpecTable kSpecTables[] = {
-    {ge::kSpecsForward, &ge::kNumSpecsForward}, {ge::kSpecsAux, &ge::kNumSpecsAux}, {ge::kSpecsFp8, &ge::kNumSpecsFp8}};
+    {ge::kSpecsForward, &ge::kNumSpecsForward}, {ge::kSpecsAux, &ge::kNumSpecsAux}, {ge::kSpecsFp8, &ge::kNumSpecsFp8},
+    {ge::kSpecsCommon, &ge::kNumSpecsCommon}};
 constexpr int kNumSpecTables = sizeof(kSpecTables) / sizeof(kSpecTables[0]);
 
 // The interpreting kernels (any program); static ones come from the tables.

@@ -46,6 +46,18 @@ using ProgRmsBwd = StaticProgram<GEMM_EPI_OP_STORE_BF16, GEMM_EPI_OP_MUL_COL_SCA
 using ProgGeluGradColSum = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16,
                                          GEMM_EPI_OP_COL_SUM>;
 
+// Common forward / backward programs outside the benchmark set.
+using ProgBias = StaticProgram<GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_STORE_BF16>;
+using ProgBiasGeluNoAmax = StaticProgram<GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_GELU_TANH, GEMM_EPI_OP_STORE_BF16>;
+using ProgBiasRelu = StaticProgram<GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_RELU, GEMM_EPI_OP_STORE_BF16>;
+using ProgBiasSilu = StaticProgram<GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_SILU, GEMM_EPI_OP_STORE_BF16>;
+using ProgAlphaBiasGelu = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_ADD_BIAS_COL, GEMM_EPI_OP_ACT_GELU_TANH,
+                                        GEMM_EPI_OP_STORE_BF16>;
+using ProgResidual = StaticProgram<GEMM_EPI_OP_ADD_RESIDUAL, GEMM_EPI_OP_STORE_BF16>;
+using ProgGeluGrad = StaticProgram<GEMM_EPI_OP_MUL_GELU_TANH_GRAD, GEMM_EPI_OP_STORE_BF16>;
+using ProgAlpha = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_STORE_BF16>;
+using ProgRowScale = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, GEMM_EPI_OP_STORE_BF16>;
+
 // One compiled program: its op list (code | pair group << 8), the operand
 // width it was compiled for and its kernels for the 1-SM and 2-SM main loops.
 struct KernelSpec {
@@ -79,6 +91,8 @@ extern const KernelSpec kSpecsAux[];
 extern const int kNumSpecsAux;
 extern const KernelSpec kSpecsFp8[];
 extern const int kNumSpecsFp8;
+extern const KernelSpec kSpecsCommon[];
+extern const int kNumSpecsCommon;
 // The interpreting kernels for 8-bit operands (1-SM, 2-SM), from the same
 // translation unit as kSpecsFp8.
 extern const void* const kDynamicFp8[2];

@@ -510,3 +510,33 @@ def test_rmsnorm_backward_empty_shapes():
     api.rmsnorm_backward(none, none, torch.ones(4, device=DEV), torch.ones(4, device=DEV), dx=none)
     torch.cuda.synchronize()
     assert torch.all(dw == 0)
+
+
+COMMON_PROGRAMS = [
+    ["bias", "store_bf16"], ["bias", "gelu_tanh", "store_bf16"], ["bias", "relu", "store_bf16"],
+    ["bias", "silu", "store_bf16"], ["alpha", "bias", "gelu_tanh", "store_bf16"], ["residual", "store_bf16"],
+    ["gelu_tanh_grad", "store_bf16"], ["alpha", "store_bf16"], ["row_scale", "store_bf16"],
+]
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("program", COMMON_PROGRAMS, ids=lambda p: ",".join(p))
+def test_common_static_programs(program, variant):
+    """The common programs compiled as static kernels (and, for comparison,
+    through the interpreter) against the oracle."""
+    M, N, K = 300, 528, 200
+    gen = torch.Generator(device=DEV).manual_seed(130)
+    A = (torch.randn(M, K, generator=gen, device=DEV) * 0.3).to(torch.bfloat16)
+    B = (torch.randn(N, K, generator=gen, device=DEV) * 0.3).to(torch.bfloat16)
+    bias = torch.randn(N, generator=gen, device=DEV) * 0.2
+    rs = torch.rand(M, generator=gen, device=DEV) + 0.5
+    aux = torch.randn(M, N, generator=gen, device=DEV).to(torch.bfloat16)
+    plan = api.Plan(M, N, K, program, b_layout="nk")
+    out = api.allocate_outputs(plan, DEV)
+    api.run_program(plan, A, B, out, alpha=1.25, bias=bias, row_scale=rs, aux=aux, debug_flags=VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert plan.query_status(out.workspace) == 0
+    r = oracle.Problem(bits(A), bits(B), program, b_is_nk=True, alpha=1.25, bias=bias.cpu().numpy(),
+                       row_scale=rs.cpu().numpy(), residual=bits(aux) if "residual" in program else None,
+                       preact=bits(aux) if "gelu_tanh_grad" in program else None).rows()
+    check_bf16(bits(out.C), r["y"])
