@@ -346,7 +346,7 @@ def run_ours(args, world, rank, local):
     if fin:
         # The GEMM's own launch time (the roofline's kernel) from events
         # around each GEMM launch inside the timed loop.
-        seconds, gemm_seconds = time_steps_split(gemm, fin, args.steps, stream)
+        seconds, gemm_seconds, fin_seconds = time_steps_split(gemm, fin, args.steps, stream)
     elif w.flops < LATENCY_BOUND_FLOPS:
         # A launch-latency-bound problem: the K steps are captured once in a
         # CUDA graph and the replay is timed, so host launch cost is excluded.
@@ -436,6 +436,17 @@ def run_ours(args, world, rank, local):
     roofline = {"bound": "tensor", "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": fused_tflops / peak, "traffic": traffic, "peak_source": peak_source,
                 "algorithmic_flops_per_launch": flops}
+    second_pass = None
+    if fin:
+        # The memory-bound second pass, against the measured copy bandwidth
+        # (its time includes the clearing of dw that precedes each launch).
+        t_fin = fin_seconds / args.steps
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        nbytes = finish_bytes(w)
+        second_pass = {"kernel": "rmsnorm_bwd_kernel", "bound": "hbm", "us_per_launch": t_fin * 1e6,
+                       "achieved": nbytes / t_fin / 1e9, "peak": hbm, "unit": "GB/s",
+                       "frac": nbytes / t_fin / 1e9 / hbm, "algorithmic_bytes_per_launch": nbytes,
+                       "peak_source": "%s HBM copy" % src}
     cpu = None
     if not args.no_cpu:
         host = synth.make_inputs(w, "cpu")
@@ -456,6 +467,7 @@ def run_ours(args, world, rank, local):
                        sum(t.numel() * t.element_size() for t in (inp.A, inp.B, inp.B2, inp.aux, inp.bias)
                            if t is not None) // 2 ** 20 + plan.M * plan.n_out * 2 // 2 ** 20)},
         "roofline": roofline,
+        **({"second_pass": second_pass} if second_pass else {}),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
@@ -463,6 +475,12 @@ def run_ours(args, world, rank, local):
         **extras,
     }
     print(json.dumps(line), flush=True)
+
+
+def finish_bytes(w):
+    """Algorithmic bytes of one RMSNorm-backward second pass: dy and x read
+    and dx written (bf16), w, S and r read and dw written (fp32)."""
+    return 3 * w.M * w.n_out * 2 + 4 * (2 * w.n_out + 2 * w.M)
 
 
 def make_finish(w, inp, out, dev):
@@ -486,20 +504,23 @@ def make_finish(w, inp, out, dev):
 
 def time_steps_split(first, second, steps, stream):
     """Times `steps` of first(); second() with events around the whole loop
-    and around each first(); returns (total seconds, seconds in first())."""
+    and around each call; returns (total seconds, seconds in first(),
+    seconds in second())."""
     import torch
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    marks = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     start.record(stream)
-    for a, b in marks:
+    for a, b, c in marks:
         a.record(stream)
         first()
         b.record(stream)
         second()
+        c.record(stream)
     end.record(stream)
     end.synchronize()
-    return start.elapsed_time(end) / 1e3, sum(a.elapsed_time(b) for a, b in marks) / 1e3
+    return (start.elapsed_time(end) / 1e3, sum(a.elapsed_time(b) for a, b, _ in marks) / 1e3,
+            sum(b.elapsed_time(c) for _, b, c in marks) / 1e3)
 
 
 def measure_e2e(plan, w, inp, out, kw, dev, steps, world, fin=None):

@@ -53,6 +53,7 @@ struct DeviceState {
   bool ready = false;
   int cc_major = 0, cc_minor = 0, sms = 0;
   int pair_clusters = 0;  // CTA pairs of the 2-SM kernel that fit on the GPU at once
+  int rb_blocks[2] = {0, 0};  // resident blocks per SM of the RMSNorm backward pass (without, with add)
   void* no_alloc_scratch = nullptr;  // device address of g_no_alloc_scratch
 };
 
@@ -132,6 +133,14 @@ gemm_epi_status device_state(DeviceState** out, int* dev_out) {
       e = cudaOccupancyMaxActiveClusters(&clusters, kDynamic2, &cfg);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
       d.pair_clusters = clusters;
+      for (int add = 0; add < 2; ++add) {
+        const void* k = add ? reinterpret_cast<const void*>(&ge::rmsnorm_bwd_kernel<true>)
+                            : reinterpret_cast<const void*>(&ge::rmsnorm_bwd_kernel<false>);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.rb_blocks[add], k, ge::RB_THREADS,
+                                                          ge::rb_ring_bytes(add != 0));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        d.rb_blocks[add] = std::max(1, d.rb_blocks[add]);
+      }
     }
     if (!g_encode) {
       void* fn = nullptr;
@@ -840,12 +849,17 @@ gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bwd_args* a, vo
   p.dx = static_cast<uint16_t*>(a->dx);
   p.ld_dx = a->ld_dx;
   p.dw = a->dw;
-  // About 8 blocks of 256 threads per SM, striding over the rows.
+  // One wave of resident blocks, striding over the rows.
+  const bool add = p.add != nullptr;
   const int64_t col_blocks = (a->N + ge::RB_COLS - 1) / ge::RB_COLS;
-  const int64_t want = std::max<int64_t>(1, 8LL * dev->sms / col_blocks);
+  const int64_t want = std::max<int64_t>(1, static_cast<int64_t>(dev->rb_blocks[add]) * dev->sms / col_blocks);
   const int64_t row_blocks = std::min<int64_t>(want, (a->M + ge::RB_TY - 1) / ge::RB_TY);
   const dim3 grid(static_cast<unsigned>(col_blocks), static_cast<unsigned>(std::min<int64_t>(row_blocks, 65535)));
-  ge::rmsnorm_bwd_kernel<<<grid, dim3(ge::RB_TX, ge::RB_TY), 0, st>>>(p);
+  const dim3 block(ge::RB_TX, ge::RB_TY);
+  if (add)
+    ge::rmsnorm_bwd_kernel<true><<<grid, block, ge::rb_ring_bytes(true), st>>>(p);
+  else
+    ge::rmsnorm_bwd_kernel<false><<<grid, block, ge::rb_ring_bytes(false), st>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? GEMM_EPI_OK : cuda_fail(e, "launch of the RMSNorm backward kernel");
 }

@@ -31,7 +31,10 @@ def _bf16(t):
     return t.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("M,N,ld", [(300, 1003, 1008), (257, 4096, 4096), (1, 8, 8), (40, 2048 + 24, 2080)])
+# The last two shapes give each thread many rows (wide rows leave few row
+# blocks; tall narrow ones many), so the per-thread copy ring wraps often.
+@pytest.mark.parametrize("M,N,ld", [(300, 1003, 1008), (257, 4096, 4096), (1, 8, 8), (40, 2048 + 24, 2080),
+                                    (1000, 32768 + 24, 32800), (20000, 259, 272)])
 @pytest.mark.parametrize("with_w,with_add", [(True, True), (False, False)])
 def test_second_pass_matches_oracle(M, N, ld, with_w, with_add):
     g = torch.Generator(device=DEV).manual_seed(100 + N)
