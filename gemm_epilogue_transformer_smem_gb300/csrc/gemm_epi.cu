@@ -325,7 +325,7 @@ gemm_epi_status validate(gemm_epi_plan& P) {
   }
   if (P.uses_residual && P.uses_preact)
     return fail(GEMM_EPI_ERR_UNSUPPORTED, "ops reading residual and ops reading preact in one program need two "
-                                          "auxiliary tensors; this build reads one");
+                                          "auxiliary tensors; this library reads one");
   if (P.uses_residual || P.uses_preact) P.flags |= ge::F_AUX;
   if (d.K == 0) P.flags |= ge::F_ZERO_ACC;
   P.n_out = P.pair_at >= 0 ? d.N / 2 : P.expand_at >= 0 ? 2 * d.N : d.N;
@@ -745,8 +745,13 @@ gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_epi_args* arg
   dim3 grid(static_cast<unsigned>((h->n_out + ge::UF_COLS - 1) / ge::UF_COLS),
             static_cast<unsigned>((d.M + ge::UF_ROWS - 1) / ge::UF_ROWS));
   if (grid.y > 65535u) return fail(GEMM_EPI_ERR_UNSUPPORTED, "separate pass: M too large for its grid");
-  ge::unfused_epilogue_kernel<<<grid, ge::UF_THREADS, 0, st>>>(u);
-  cudaError_t e = cudaGetLastError();
+  // The program's compiled separate pass, else the interpreting one.
+  const void* uk = (h->spec && h->spec->kernel_unfused && !(args->debug_flags & GEMM_EPI_DEBUG_FORCE_INTERPRETER))
+                       ? h->spec->kernel_unfused
+                       : reinterpret_cast<const void*>(&ge::unfused_epilogue_kernel<ge::DynamicProgram>);
+  void* uargs[] = {&u};
+  cudaError_t e = cudaLaunchKernel(uk, grid, dim3(ge::UF_THREADS), uargs, 0, st);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the separate epilogue pass");
   if ((h->flags & ge::F_ROW) && (h->flags & ge::F_RSQRT)) {
     const int threads = 256;

@@ -7,6 +7,7 @@
 #pragma once
 
 #include "fused_kernel.cuh"
+#include "unfused_kernel.cuh"
 
 namespace ge {
 
@@ -59,7 +60,9 @@ using ProgAlpha = StaticProgram<GEMM_EPI_OP_SCALE_ALPHA, GEMM_EPI_OP_STORE_BF16>
 using ProgRowScale = StaticProgram<GEMM_EPI_OP_MUL_ROW_SCALE, GEMM_EPI_OP_STORE_BF16>;
 
 // One compiled program: its op list (code | pair group << 8), the operand
-// width it was compiled for and its kernels for the 1-SM and 2-SM main loops.
+// width it was compiled for, its kernels for the 1-SM and 2-SM main loops and
+// its separate-pass kernel for the unfused baseline (NULL if the pass does
+// not cover the program).
 struct KernelSpec {
   const char* name;
   int n_ops;
@@ -67,6 +70,7 @@ struct KernelSpec {
   int in8;  // 1: 8-bit operands
   const void* kernel_1sm;
   const void* kernel_2sm;
+  const void* kernel_unfused;
 };
 
 template <class Prog, int IN8, int... Is>
@@ -76,7 +80,8 @@ inline KernelSpec make_spec(const char* name, std::integer_sequence<int, Is...>)
                     {(Prog::code_of(Is) | (Prog::arg_of(Is) << 8))...},
                     IN8,
                     reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<1, Prog, IN8>),
-                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<2, Prog, IN8>)};
+                    reinterpret_cast<const void*>(&fused_gemm_epilogue_kernel<2, Prog, IN8>),
+                    unfused_kernel_for<Prog>()};
 }
 
 template <class Prog, int IN8 = 0>

@@ -9,6 +9,10 @@
 // Layout of the work: a 256-thread block covers 32 rows x 256 output columns;
 // warp w takes rows w, w+8, w+16, w+24 of the block, lane l takes 8
 // consecutive output columns (16-byte loads and stores, coalesced per warp).
+//
+// Like the fused kernel, the pass comes in two forms: compiled for one
+// static program (the op dispatch, pair and expansion groups fold at compile
+// time), and interpreting the op list of any other program.
 #pragma once
 
 #include "fused_kernel.cuh"
@@ -49,9 +53,11 @@ __device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
 }
 
 // Point-wise op on 8 values whose columns are col0..col0+7 (< ncols checked).
-__device__ __forceinline__ void uf_pointwise(const EpiOpDev& op, float (&v)[8], const UnfusedParams& p,
-                                             int col0, int ncols, float rs) {
-  switch (op.code) {
+// `code` is an int, or a std::integral_constant whose switch folds.
+template <class CodeT>
+__device__ __forceinline__ void uf_pointwise(CodeT code, float (&v)[8], const UnfusedParams& p, int col0, int ncols,
+                                             float rs) {
+  switch (static_cast<int>(code)) {
     case GEMM_EPI_OP_SCALE_ALPHA:
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] *= p.alpha;
@@ -102,16 +108,36 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* src, bool full, int v
   }
 }
 
+// Runs f(std::integral_constant<int, code>) for the static program's ops
+// [Begin, End), or f(code) for the interpreted ops [begin, end).
+template <class Prog, int Begin, int End, class F>
+__device__ __forceinline__ void uf_ops(const UnfusedParams& p, int begin, int end, F&& f) {
+  if constexpr (Prog::is_static) {
+    static_for<Begin, End>([&](auto I) { f(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}); });
+  } else {
+    for (int k = begin; k < end; ++k) f(p.ops[k].code);
+  }
+}
+
+template <class Prog>
 __global__ void __launch_bounds__(UF_THREADS)
     unfused_epilogue_kernel(const __grid_constant__ UnfusedParams p) {
+  constexpr bool kStatic = Prog::is_static;
+  // Positions of the pair / expanding op in a static program (0 if absent).
+  constexpr int kPairAt = prog_pair_at<Prog>() < 0 ? 0 : prog_pair_at<Prog>();
+  constexpr int kExpandAt = prog_expand_at<Prog>() < 0 ? 0 : prog_expand_at<Prog>();
   __shared__ float col_part[UF_THREADS / 32][UF_COLS];
   __shared__ uint32_t amax_part[UF_THREADS / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_base = blockIdx.y * UF_ROWS;
   const int c0 = blockIdx.x * UF_COLS + lane * 8;  // first output column of this thread
-  const bool paired = p.pair_at >= 0;
-  const bool expand = p.expand_at >= 0;
-  const int op_begin = paired ? p.pair_at + 1 : expand ? p.expand_at + 1 : 0;
+  const int pair_at = kStatic ? prog_pair_at<Prog>() : p.pair_at;
+  const int expand_at = kStatic ? prog_expand_at<Prog>() : p.expand_at;
+  const bool paired = pair_at >= 0;
+  const bool expand = expand_at >= 0;
+  const int op_begin = paired ? pair_at + 1 : expand ? expand_at + 1 : 0;
+  const int n_ops = kStatic ? prog_n<Prog>() : p.n_ops;
+  const uint32_t flags = kStatic ? static_flags<Prog>() : p.flags;
   const int valid = min(8, p.n_out - c0);
   const bool full = valid == 8;
 
@@ -130,14 +156,14 @@ __global__ void __launch_bounds__(UF_THREADS)
       const int a0 = c0 / 2;
 #pragma unroll
       for (int j = 0; j < 4; ++j) dh[j] = a0 + j < p.N ? bf16_bits_to_f(p.acc[m * p.ld_acc + a0 + j]) : 0.0f;
-      for (int k = 0; k < p.expand_at; ++k) {
+      uf_ops<Prog, 0, kExpandAt>(p, 0, expand_at, [&](auto code) {
         float h[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) h[j] = j < 4 ? dh[j] : 0.0f;
-        uf_pointwise(p.ops[k], h, p, a0, min(p.N, a0 + 4), rs);
+        uf_pointwise(code, h, p, a0, min(p.N, a0 + 4), rs);
 #pragma unroll
         for (int j = 0; j < 4; ++j) dh[j] = h[j];
-      }
+      });
     } else if (!paired) {
       load8_bf16(p.acc + m * p.ld_acc + c0, full, valid, v);
     } else {
@@ -148,42 +174,41 @@ __global__ void __launch_bounds__(UF_THREADS)
       const int avalid = min(16, p.N - a0);
       load8_bf16(p.acc + m * p.ld_acc + a0, avalid >= 8, max(0, min(8, avalid)), lo);
       load8_bf16(p.acc + m * p.ld_acc + a0 + 8, avalid >= 16, max(0, avalid - 8), hi);
+      uf_ops<Prog, 0, kPairAt>(p, 0, pair_at, [&](auto code) {
+        uf_pointwise(code, lo, p, a0, p.N, rs);
+        uf_pointwise(code, hi, p, a0 + 8, p.N, rs);
+      });
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         a[j] = lo[j];
         a[8 + j] = hi[j];
       }
-      for (int k = 0; k < p.pair_at; ++k) {
-        float h0[8], h1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          h0[j] = a[j];
-          h1[j] = a[8 + j];
-        }
-        uf_pointwise(p.ops[k], h0, p, a0, p.N, rs);
-        uf_pointwise(p.ops[k], h1, p, a0 + 8, p.N, rs);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a[j] = h0[j];
-          a[8 + j] = h1[j];
-        }
-      }
       // Groups g <= 8 keep the pair inside these 16 columns (checked on the host).
+      if constexpr (kStatic) {
+        constexpr int g = prog_pair_g<Prog>();
+        static_assert(g <= 8, "the separate pass handles pair groups up to 8");
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int g = p.pair_g;
-        const int gate = (j / g) * 2 * g + (j % g);
-        float ga = 0.0f, ua = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          if (q == gate) ga = a[q];
-          if (q == gate + g) ua = a[q];
+        for (int j = 0; j < 8; ++j) {
+          const int gate = (j / g) * 2 * g + (j % g);
+          v[j] = (prog_pair_silu<Prog>() ? silu_f(a[gate]) : a[gate]) * a[gate + g];
         }
-        v[j] = (p.pair_silu ? silu_f(ga) : ga) * ua;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int g = p.pair_g;
+          const int gate = (j / g) * 2 * g + (j % g);
+          float ga = 0.0f, ua = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            if (q == gate) ga = a[q];
+            if (q == gate + g) ua = a[q];
+          }
+          v[j] = (p.pair_silu ? silu_f(ga) : ga) * ua;
+        }
       }
     }
     float x[8];
-    if (p.flags & F_AUX) {
+    if (flags & F_AUX) {
       load8_bf16(p.aux + m * p.ld_aux + c0, full, valid, x);
     } else {
 #pragma unroll
@@ -192,28 +217,40 @@ __global__ void __launch_bounds__(UF_THREADS)
     if (expand) {
       // Groups g <= 4 keep whole gate / up pairs inside these 8 outputs
       // (checked on the host).
-      const int g = p.expand_g;
+      if constexpr (kStatic) {
+        constexpr int g = prog_expand_g<Prog>();
+        static_assert(g <= 4, "the separate pass handles DSWIGLU groups up to 4");
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int gate = (j / (2 * g)) * 2 * g + j % g;
-        const int jl = (j / (2 * g)) * g + j % g;
-        float gt = 0.0f, up = 0.0f, d = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (q == gate) gt = x[q];
-          if (q == gate + g) up = x[q];
+        for (int j = 0; j < 8; ++j) {
+          const int gate = (j / (2 * g)) * 2 * g + j % g;
+          const int jl = (j / (2 * g)) * g + j % g;
+          const float gt = x[gate], up = x[gate + g], d = dh[jl];
+          const float sg = sigmoid_f(gt);
+          v[j] = (j % (2 * g)) < g ? d * up * (sg * fmaf(gt, 1.0f - sg, 1.0f)) : d * (gt * sg);
         }
+      } else {
+        const int g = p.expand_g;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q == jl) d = dh[q];
-        const float sg = sigmoid_f(gt);
-        v[j] = (j % (2 * g)) < g ? d * up * (sg * fmaf(gt, 1.0f - sg, 1.0f)) : d * (gt * sg);
+        for (int j = 0; j < 8; ++j) {
+          const int gate = (j / (2 * g)) * 2 * g + j % g;
+          const int jl = (j / (2 * g)) * g + j % g;
+          float gt = 0.0f, up = 0.0f, d = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (q == gate) gt = x[q];
+            if (q == gate + g) up = x[q];
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q == jl) d = dh[q];
+          const float sg = sigmoid_f(gt);
+          v[j] = (j % (2 * g)) < g ? d * up * (sg * fmaf(gt, 1.0f - sg, 1.0f)) : d * (gt * sg);
+        }
       }
     }
     float row_ss = 0.0f;
-    for (int k = op_begin; k < p.n_ops; ++k) {
-      const EpiOpDev op = p.ops[k];
-      switch (op.code) {
+    auto run_op = [&](auto code) {
+      switch (static_cast<int>(code)) {
         case GEMM_EPI_OP_ADD_RESIDUAL:
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] += x[j];
@@ -274,18 +311,19 @@ __global__ void __launch_bounds__(UF_THREADS)
           for (int j = 0; j < 8; ++j) colacc[j] += v[j];
           break;
         default:
-          uf_pointwise(op, v, p, c0, p.n_out, rs);
+          uf_pointwise(code, v, p, c0, p.n_out, rs);
           break;
       }
-    }
-    if (p.flags & F_ROW) {
+    };
+    uf_ops<Prog, prog_post_begin<Prog>(), prog_n<Prog>()>(p, op_begin, n_ops, run_op);
+    if (flags & F_ROW) {
 #pragma unroll
       for (int s = 16; s >= 1; s >>= 1) row_ss += __shfl_xor_sync(0xffffffffu, row_ss, s);
       if (lane == 0) atomicAdd(p.row_out + m, row_ss);
     }
   }
 
-  if (p.flags & F_COL) {
+  if (flags & F_COL) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) col_part[warp][lane * 8 + j] = colacc[j];
     __syncthreads();
@@ -295,7 +333,7 @@ __global__ void __launch_bounds__(UF_THREADS)
     for (int w = 0; w < UF_THREADS / 32; ++w) s += col_part[w][threadIdx.x];
     if (col < p.n_out) atomicAdd(p.col_out + col, s);
   }
-  if (p.flags & F_AMAX) {
+  if (flags & F_AMAX) {
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, s));
     if (lane == 0) amax_part[warp] = amax_bits;
@@ -308,8 +346,21 @@ __global__ void __launch_bounds__(UF_THREADS)
   }
 }
 
+// The separate pass of a static program, or NULL where the pass does not
+// cover the program (pair groups above 8, DSWIGLU groups above 4).
+template <class Prog>
+inline const void* unfused_kernel_for() {
+  if constexpr (Prog::pair_at() >= 0 && Prog::pair_g() > 8) {
+    return nullptr;
+  } else if constexpr (Prog::expand_at() >= 0 && Prog::expand_g() > 4) {
+    return nullptr;
+  } else {
+    return reinterpret_cast<const void*>(&unfused_epilogue_kernel<Prog>);
+  }
+}
+
 // row_out[m] = 1 / sqrt(row_out[m] / n + eps) for the separate pass.
-__global__ void row_rms_finalize_kernel(float* row_out, int M, float inv_n, float eps) {
+static __global__ void row_rms_finalize_kernel(float* row_out, int M, float inv_n, float eps) {
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m < M) row_out[m] = 1.0f / sqrtf(fmaf(row_out[m], inv_n, eps));
 }

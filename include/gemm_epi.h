@@ -108,7 +108,7 @@ typedef enum gemm_epi_status {
     GEMM_EPI_OK = 0,
     GEMM_EPI_ERR_INVALID_VALUE = 1, /* bad size, NULL where required, bad program */
     GEMM_EPI_ERR_MISALIGNED = 2,    /* pointer or stride breaks the 16-byte TMA rule */
-    GEMM_EPI_ERR_UNSUPPORTED = 3,   /* a legal program this build does not implement */
+    GEMM_EPI_ERR_UNSUPPORTED = 3,   /* a legal program this library does not implement */
     GEMM_EPI_ERR_ARCH = 4,          /* current device is not compute capability 10.x */
     GEMM_EPI_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
     GEMM_EPI_ERR_TIMEOUT = 6,       /* a bounded in-kernel wait ran out */

@@ -81,11 +81,14 @@ def unfused_oracle(w, inp):
     return p
 
 
+@pytest.mark.parametrize("form", ["static", "interp"])
 @pytest.mark.parametrize("name,M,N,K", [s for s in SMALL_SHAPES[1:] if s[0] != "swiglu2w"])
-def test_small_unfused_baseline(name, M, N, K):
+def test_small_unfused_baseline(name, M, N, K, form):
+    """The separate pass, compiled for the program and interpreted."""
     w = small(name, M, N, K)
     inp = synth.make_inputs(w, DEV)
-    plan, out = run_cuda(w, inp, unfused=True)
+    flags = native.GEMM_EPI_DEBUG_FORCE_INTERPRETER if form == "interp" else 0
+    plan, out = run_cuda(w, inp, unfused=True, debug_flags=flags)
     p = unfused_oracle(w, inp)
     compare_rows(w, inp, out, oracle_p=p)
     if out.col_out is not None:
