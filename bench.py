@@ -41,7 +41,7 @@ KERNEL_NAME = "fused_gemm_epilogue_kernel"
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="swiglu")
@@ -260,7 +260,8 @@ def run_reference(args, world, rank):
         return
     w = synth.WORKLOADS[args.workload]
     inp = host_inputs(w)
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # about 150 s of oracle work over the whole run, whatever the step count
+    per_step = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     # size one step once, then run warmup + steps of that size
     _, rows, threads, _ = oracle_rows_sample(w, inp, per_step)
     prob = oracle_problem(w, inp)
