@@ -453,6 +453,7 @@ def run_ours(args, world, rank, local):
         second_pass = {"kernel": "rmsnorm_bwd_kernel", "bound": "hbm", "us_per_launch": t_fin * 1e6,
                        "achieved": nbytes / t_fin / 1e9, "peak": hbm, "unit": "GB/s",
                        "frac": nbytes / t_fin / 1e9 / hbm, "algorithmic_bytes_per_launch": nbytes,
+                       "traffic": profiled_traffic(w.name + ":second_pass"),
                        "peak_source": "%s HBM copy" % src}
     cpu = None
     if not args.no_cpu:
