@@ -206,14 +206,17 @@ def oracle_problem(w, inp):
     def scalar(t):
         return 1.0 if t is None else float(t.item())
 
-    aux = synth.bf16_bits(inp.aux) if inp.aux is not None else None
-    return oracle.Problem(operand(inp.A), operand(inp.B), list(w.program), b_is_nk=(w.b_layout == "nk"),
+    first = (lambda t: None if t is None else t[0]) if w.batch > 1 else (lambda t: t)  # batch 0
+    aux = synth.bf16_bits(first(inp.aux)) if inp.aux is not None else None
+    row_scale = None if inp.row_scale is None else inp.row_scale.cpu().numpy()[:w.M]
+    return oracle.Problem(operand(first(inp.A)), operand(first(inp.B)), list(w.program), b_is_nk=(w.b_layout == "nk"),
                           alpha=inp.alpha, bias=None if inp.bias is None else inp.bias.cpu().numpy(),
                           residual=aux if w.aux == "residual" else None,
                           preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
                           B2=operand(inp.B2), a_type=w.in_type, b_type=w.in_type,
                           a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv),
-                          col_scale=None if inp.col_scale is None else inp.col_scale.cpu().numpy())
+                          col_scale=None if inp.col_scale is None else inp.col_scale.cpu().numpy(),
+                          row_scale=row_scale)
 
 
 def oracle_step(w, inp, prob, rows):
@@ -273,13 +276,14 @@ def run_reference(args, world, rank):
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K * args.steps
     value = flops / dt / 1e12
-    sample = "%d of %d rows (all %d columns, K=%d) per step" % (rows, w.M, w.n_out, w.K)
+    sample = "%d of %d rows%s (all %d columns, K=%d) per step" % (
+        rows, w.M, " of the first of %d problems" % w.batch if w.batch > 1 else "", w.n_out, w.K)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "program": list(w.program)},
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "program": list(w.program)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -312,12 +316,12 @@ def run_ours(args, world, rank, local):
     w = synth.WORKLOADS[args.workload]
     inp = synth.make_inputs(w, dev)
     types = dict(a_type=w.in_type, b_type=w.in_type)
-    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, **types)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
     out = api.allocate_outputs(plan, dev)
     stream = torch.cuda.current_stream(dev)
     scales = dict(a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv)
     kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2,
-              col_scale=inp.col_scale, **scales)
+              col_scale=inp.col_scale, row_scale=inp.row_scale, **scales)
     fin = make_finish(w, inp, out, dev)
     launches_per_step = 2 if fin else 1
 
@@ -380,7 +384,7 @@ def run_ours(args, world, rank, local):
         # Fused, bare GEMM (same main loop, store-only program) and unfused
         # (bare GEMM + separate epilogue pass) timed in interleaved rounds so
         # that all three see the same clock and power state; medians.
-        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual, **types)
+        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
         bare_out = api.allocate_outputs(bare, dev)
 
         def bare_step():
@@ -465,8 +469,8 @@ def run_ours(args, world, rank, local):
         host = synth.make_inputs(w, "cpu")
         tf, rows, threads, dt = oracle_rows_sample(w, host, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": "%d of %d rows x all %d output columns, K=%d (%.1f s)" % (
-                   rows, w.M, w.n_out, w.K, dt)}
+               "sample": "%d of %d rows%s x all %d output columns, K=%d (%.1f s)" % (
+                   rows, w.M, " of the first of %d problems" % w.batch if w.batch > 1 else "", w.n_out, w.K, dt)}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -474,7 +478,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "timing": "CUDA-graph replay of the %d steps" % args.steps if graph is not None else "stream launches",
         "us_per_step": seconds / args.steps * 1e6,
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "b_layout": w.b_layout,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "b_layout": w.b_layout,
                    "program": list(w.program), "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: inputs + output (%d MB) exceed the 129 MB L2" % (
                        sum(t.numel() * t.element_size() for t in (inp.A, inp.B, inp.B2, inp.aux, inp.bias)
@@ -495,7 +499,7 @@ def separate_pass_bytes(w):
     that stored the bf16 accumulator: that accumulator and any auxiliary
     tensor read, the program's outputs written (reduction vectors ignored)."""
     prog = [op.partition(":")[0] for op in w.program]
-    rows = w.M
+    rows = w.batch * w.M
     b = rows * w.N * 2
     if w.aux:
         b += rows * w.n_out * 2
@@ -564,9 +568,9 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world, fin=None):
     import torch
     from gemm_epilogue_transformer_smem_gb300 import api
 
-    names = ("A", "B", "bias", "aux", "B2", "a_scale_inv", "b_scale_inv", "col_scale", "row_stat")
+    names = ("A", "B", "bias", "aux", "B2", "a_scale_inv", "b_scale_inv", "col_scale", "row_stat", "row_scale")
     src = dict(zip(names, (inp.A, inp.B, inp.bias, inp.aux, inp.B2, inp.a_scale_inv, inp.b_scale_inv,
-                           inp.col_scale, inp.row_stat)))
+                           inp.col_scale, inp.row_stat, inp.row_scale)))
     h = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in src.items()}
 
     def buffers():
@@ -592,7 +596,8 @@ def measure_e2e(plan, w, inp, out, kw, dev, steps, world, fin=None):
         d = b["d"]
         api.run_program(plan, d["A"], d["B"], b["o"], alpha=kw["alpha"], fp8_scale=kw["fp8_scale"],
                         bias=d["bias"], aux=d["aux"], B2=d["B2"], a_scale_inv=d["a_scale_inv"],
-                        b_scale_inv=d["b_scale_inv"], col_scale=d["col_scale"], stream=stream)
+                        b_scale_inv=d["b_scale_inv"], col_scale=d["col_scale"], row_scale=d["row_scale"],
+                        stream=stream)
         if b["f"]:
             b["f"](aux=d["aux"], w_=d["col_scale"], s_=d["row_stat"])
 

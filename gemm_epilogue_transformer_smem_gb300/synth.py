@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five GEMM + epilogue workloads.
+"""Seeded synthetic inputs for the GEMM + epilogue workloads.
 
 This module holds shapes, value distributions and random draws only -- none
 of the method's arithmetic.  Both the CUDA path and the CPU oracle read the
@@ -42,8 +42,19 @@ them; "N(0, s)" has standard deviation s):
             scale 448/4), dequantised by 1/112.  B: a weight stored N x K,
             N(0,1)/sqrt(K), as e4m3 codes at scale 112 * sqrt(K) (448/4 of its
             own standard deviation), dequantised by the reciprocal.
+  rmsswiglu the RMSNorm-consuming up-projection: the swiglu workload's GEMM
+            with its rows scaled by the previous layer's S before the pair
+            op, out = silu(S*gate) * (S*up).  A (the unnormalised residual
+            stream) 8192x4096 N(0,1); B 4096x28672 N(0, 0.02); S fp32
+            1 + N(0, 0.05) per row.
+  rmsglu    the same with the RMSNorm-MLP's plain product, out = (S*gate) *
+            (S*up).
+  moe8      eight independent SwiGLU up-projections in one launch (one per
+            expert, each with its own weights): per expert A 2048x4096
+            N(0,1), B 4096x28672 N(0, 0.02).
 
-Draw order per workload: A, B, bias, residual / preact, B2, column scale, S.  Each tensor is drawn
+Draw order per workload: A, B, bias, residual / preact, B2, column scale, S,
+row scale.  A batched workload draws each tensor for every batch at once.  Each tensor is drawn
 in fp32 with ``torch.randn`` from one generator seeded with 1000 + index,
 scaled, then cast to bf16 (round to nearest even); bias stays fp32.  FP8
 operands are multiplied by their quantisation scale, clamped to the format's
@@ -82,6 +93,8 @@ class Workload:
     b_qscale: float = 1.0
     col_scale_std: Optional[float] = None   # column scale drawn as 1 + N(0, std)
     finish: Optional[str] = None            # a second pass after the GEMM ("rmsnorm_backward")
+    row_scale_std: Optional[float] = None   # row scale (the consumed S) drawn as 1 + N(0, std)
+    batch: int = 1                          # independent problems of this shape in one launch
     notes: str = ""
 
     @property
@@ -93,7 +106,7 @@ class Workload:
 
     @property
     def flops(self) -> int:
-        return 2 * self.M * self.N * self.K
+        return 2 * self.batch * self.M * self.N * self.K
 
     def scaled(self, M: int, N: int, K: int, name: Optional[str] = None) -> "Workload":
         """Same program and distributions at another shape.  Standard
@@ -139,6 +152,12 @@ WORKLOADS = {
                       a_std=0.1, b_std=1 / math.sqrt(8192), bias_std=0.1, alpha=0.5,
                       fp8_scale=448.0 / 4.0, in_type="e4m3", a_relu=True, a_qscale=112.0,
                       b_qscale=112.0 * math.sqrt(8192)),
+    "rmsswiglu": Workload("rmsswiglu", 9, 8192, 28672, 4096, "kn", ("row_scale", "pair_swiglu", "store_bf16"),
+                          a_std=1.0, b_std=0.02, row_scale_std=0.05),
+    "rmsglu": Workload("rmsglu", 10, 8192, 28672, 4096, "kn", ("row_scale", "pair_mul", "store_bf16"),
+                       a_std=1.0, b_std=0.02, row_scale_std=0.05),
+    "moe8": Workload("moe8", 11, 2048, 28672, 4096, "kn", ("pair_swiglu", "store_bf16"),
+                     a_std=1.0, b_std=0.02, batch=8),
 }
 
 BY_INDEX = {w.index: w for w in WORKLOADS.values()}
@@ -157,6 +176,7 @@ class Inputs:
     b_scale_inv: Optional[torch.Tensor] = None
     col_scale: Optional[torch.Tensor] = None    # fp32, one per output column
     row_stat: Optional[torch.Tensor] = None     # fp32, one per row (the forward's S)
+    row_scale: Optional[torch.Tensor] = None    # fp32, one per row (batch x M): the consumed S
     extra: dict = field(default_factory=dict)
 
 
@@ -190,18 +210,21 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs
         lim = torch.finfo(fmt).max
         return (t * qscale).clamp_(-lim, lim).to(fmt).view(torch.uint8)
 
-    A = operand((w.M, w.K), w.a_std, w.a_qscale, w.a_relu)
+    lead = (w.batch,) if w.batch > 1 else ()
+    A = operand(lead + (w.M, w.K), w.a_std, w.a_qscale, w.a_relu)
     nbc = w.N // 2 if w.dual else w.N
-    B = operand((w.K, nbc) if w.b_layout == "kn" else (nbc, w.K), w.b_std, w.b_qscale)
+    B = operand(lead + ((w.K, nbc) if w.b_layout == "kn" else (nbc, w.K)), w.b_std, w.b_qscale)
     nb = _bias_len(w)
     bias = draw((nb,), w.bias_std, torch.float32) if nb else None
-    aux = draw((w.M, w.n_out), w.aux_std) if w.aux else None
+    aux = draw(lead + (w.M, w.n_out), w.aux_std) if w.aux else None
     B2 = operand(tuple(B.shape), w.b_std, w.b_qscale) if w.dual else None
     inp = Inputs(A=A, B=B, bias=bias, aux=aux, alpha=w.alpha, fp8_scale=w.fp8_scale, B2=B2)
     if w.col_scale_std is not None:
         inp.col_scale = 1.0 + draw((w.n_out,), w.col_scale_std, torch.float32)
     if w.finish == "rmsnorm_backward":
         inp.row_stat = 1.0 + draw((w.M,), 0.05, torch.float32)
+    if w.row_scale_std is not None:
+        inp.row_scale = 1.0 + draw((w.batch * w.M,), w.row_scale_std, torch.float32)
     if w.in_type != "bf16":
         inp.a_scale_inv = torch.tensor([1.0 / w.a_qscale], dtype=torch.float32, device=device)
         inp.b_scale_inv = torch.tensor([1.0 / w.b_qscale], dtype=torch.float32, device=device)

@@ -114,19 +114,21 @@ def oracle_problem(w: synth.Workload, inp: synth.Inputs) -> oracle.Problem:
         preact=aux if w.aux == "preact" else None, fp8_scale=inp.fp8_scale,
         B2=operand_host(inp.B2, w.in_type), a_type=w.in_type, b_type=w.in_type,
         a_scale_inv=scalar(inp.a_scale_inv), b_scale_inv=scalar(inp.b_scale_inv),
-        col_scale=None if inp.col_scale is None else inp.col_scale.detach().cpu().numpy())
+        col_scale=None if inp.col_scale is None else inp.col_scale.detach().cpu().numpy(),
+        row_scale=None if inp.row_scale is None else inp.row_scale.detach().cpu().numpy())
 
 
 def run_cuda(w: synth.Workload, inp: synth.Inputs, unfused=False, **kw):
     plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, a_type=w.in_type,
-                    b_type=w.in_type)
+                    b_type=w.in_type, batch=w.batch)
     out = api.allocate_outputs(plan, inp.A.device)
     scratch = None
     if unfused:
         scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=inp.A.device)
     api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale,
                     bias=inp.bias, aux=inp.aux, unfused_scratch=scratch, B2=inp.B2,
-                    a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv, col_scale=inp.col_scale, **kw)
+                    a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv, col_scale=inp.col_scale,
+                    row_scale=inp.row_scale, **kw)
     torch.cuda.synchronize()
     status = plan.query_status(out.workspace)
     assert status == 0, "kernel status %d" % status

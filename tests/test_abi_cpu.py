@@ -279,12 +279,12 @@ def test_binding_supplies_every_argument_a_workload_needs(lib, name):
     w = w.scaled(min(w.M, 96), min(w.N, 512), min(w.K, 128))
     inp = synth.make_inputs(w, "cpu")
     plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, a_type=w.in_type,
-                    b_type=w.in_type)
+                    b_type=w.in_type, batch=w.batch)
     out = api.allocate_outputs(plan, "cpu")
     with pytest.raises(N.GemmEpiError) as err:
         api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias,
                         aux=inp.aux, B2=inp.B2, a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv,
-                        col_scale=inp.col_scale, stream=FakeStream())
+                        col_scale=inp.col_scale, row_scale=inp.row_scale, stream=FakeStream())
     assert err.value.status in (N.GEMM_EPI_ERR_CUDA, N.GEMM_EPI_ERR_ARCH), str(err.value)
     if w.finish == "rmsnorm_backward":
         dx = torch.empty(out.C.shape, dtype=torch.bfloat16)

@@ -84,3 +84,21 @@ def test_batched_matches_per_batch_oracle(name, shared_b, variant):
         amax = max(amax, r["amax"])
     if out.amax is not None:
         check_amax(float(out.amax.item()), amax)
+
+
+def test_moe8_full_size_sampled():
+    """The moe8 workload at full size (8 experts, 2048 x 28672 x 4096 each,
+    own weights): sampled rows of every expert against its own oracle
+    problem, the last rows of the last expert among them."""
+    from gemm_epilogue_transformer_smem_gb300 import synth
+    from parity import run_cuda
+    w = synth.WORKLOADS["moe8"]
+    inp = synth.make_inputs(w, DEV)
+    plan, out = run_cuda(w, inp)
+    rng = np.random.default_rng(w.index)
+    for b in range(w.batch):
+        rows = np.unique(np.concatenate([rng.choice(w.M, 12, replace=False), [0, w.M - 1]]))
+        p = oracle.Problem(bits(inp.A[b]), bits(inp.B[b]), list(w.program))
+        r = p.rows(rows)
+        idx = torch.as_tensor(rows, device=DEV)
+        check_bf16(bits(out.C[b][idx]), r["y"], "C[%d]" % b)

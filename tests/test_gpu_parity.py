@@ -368,7 +368,8 @@ def test_graph_capture_replay_matches_eager():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu", "drmsnorm"]
+FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu", "drmsnorm",
+        "rmsswiglu", "rmsglu"]
 
 
 @pytest.mark.parametrize("name", FULL)
