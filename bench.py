@@ -465,7 +465,7 @@ def run_ours(args, world, rank, local):
                        "traffic": profiled_traffic(w.name + ":second_pass"),
                        "peak_source": "%s HBM copy" % src}
     cpu = None
-    if not args.no_cpu:
+    if not args.no_cpu and world == 1:  # the oracle baseline is timed at N = 1 only
         host = synth.make_inputs(w, "cpu")
         tf, rows, threads, dt = oracle_rows_sample(w, host, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
