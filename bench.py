@@ -33,7 +33,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 BF16 roofline; overhead vs bare GEMM"
-LATENCY_BOUND_FLOPS = 1e9  # below this a step is timed as a CUDA-graph replay
+# A step whose roofline time (the slower of its FLOPs at the bf16 peak and
+# its bytes at the copy bandwidth) is below this is timed as a CUDA-graph
+# replay, so that the host's launch cost cannot hide GPU time.
+LATENCY_BOUND_SECONDS = 200e-6
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_NAME = "fused_gemm_epilogue_kernel"
 
@@ -352,9 +355,10 @@ def run_ours(args, world, rank, local):
         # The GEMM's own launch time (the roofline's kernel) from events
         # around each GEMM launch inside the timed loop.
         seconds, gemm_seconds, fin_seconds = time_steps_split(gemm, fin, args.steps, stream)
-    elif w.flops < LATENCY_BOUND_FLOPS:
-        # A launch-latency-bound problem: the K steps are captured once in a
-        # CUDA graph and the replay is timed, so host launch cost is excluded.
+    elif roofline_seconds(w) < LATENCY_BOUND_SECONDS:
+        # A short step (launch bound, or a skinny GEMM of a few tens of
+        # microseconds): the K steps are captured once in a CUDA graph and
+        # the replay is timed, so host launch cost is excluded.
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
@@ -444,10 +448,21 @@ def run_ours(args, world, rank, local):
         peak *= 2.0
         peak_source = "%s burst bf16 (cuBLAS) x 2, the nominal dense fp8/bf16 ratio" % src
     traffic = profiled_traffic(w.name)
-    roofline = {"bound": "tensor", "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": fused_tflops / peak, "traffic": traffic, "peak_source": peak_source,
-                "algorithmic_flops_per_launch": flops}
-    if "bf16_tflops_sustained" in peaks:
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    nbytes = fused_bytes(w)
+    if nbytes / (hbm * 1e9) > flops / (peak * 1e12):
+        # Reading the operands takes longer at HBM speed than the FLOPs at
+        # tensor speed (a skinny GEMM): the HBM roofline binds.
+        t_launch = flops / (fused_tflops * 1e12)
+        roofline = {"bound": "hbm", "achieved": nbytes / t_launch / 1e9, "peak": hbm, "unit": "GB/s",
+                    "frac": nbytes / t_launch / 1e9 / hbm, "traffic": traffic,
+                    "peak_source": "%s HBM copy" % src, "algorithmic_bytes_per_launch": nbytes,
+                    "tflops": fused_tflops}
+    else:
+        roofline = {"bound": "tensor", "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": fused_tflops / peak, "traffic": traffic, "peak_source": peak_source,
+                    "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes}
+    if "bf16_tflops_sustained" in peaks and roofline["bound"] == "tensor":
         # For context: the same against the power-capped sustained figure
         # (a seconds-long loop), the regime long timed regions run in.
         sustained = float(peaks["bf16_tflops_sustained"]) * (2.0 if w.in_type != "bf16" else 1.0)
@@ -492,6 +507,31 @@ def run_ours(args, world, rank, local):
         **extras,
     }
     print(json.dumps(line), flush=True)
+
+
+def roofline_seconds(w):
+    """The slower of the step's FLOPs at the measured bf16 (or 2x for 8-bit)
+    peak and its algorithmic bytes at the measured copy bandwidth."""
+    peaks, _ = load_peaks()
+    tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * (2.0 if w.in_type != "bf16" else 1.0)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return max(w.flops / (tf * 1e12), fused_bytes(w) / (hbm * 1e9))
+
+
+def fused_bytes(w):
+    """Algorithmic bytes of one fused launch: A and B (and B2) read once,
+    any auxiliary tensor read, the program's outputs written (vectors and
+    reductions ignored)."""
+    prog = [op.partition(":")[0] for op in w.program]
+    esz = 1 if w.in_type != "bf16" else 2
+    b = w.batch * (w.M * w.K + w.K * w.N) * esz
+    if w.aux:
+        b += w.batch * w.M * w.n_out * 2
+    if "store_bf16" in prog:
+        b += w.batch * w.M * w.n_out * 2
+    if "store_e4m3" in prog:
+        b += w.batch * w.M * w.n_out
+    return b
 
 
 def separate_pass_bytes(w):

@@ -52,6 +52,9 @@ them; "N(0, s)" has standard deviation s):
   moe8      eight independent SwiGLU up-projections in one launch (one per
             expert, each with its own weights): per expert A 2048x4096
             N(0,1), B 4096x28672 N(0, 0.02).
+  decode    the swiglu workload's up-projection for one decode step of 64
+            tokens: A 64x4096 N(0,1), B 4096x28672 N(0, 0.02).  Reading B
+            dominates, so the HBM roofline binds.
 
 Draw order per workload: A, B, bias, residual / preact, B2, column scale, S,
 row scale.  A batched workload draws each tensor for every batch at once.  Each tensor is drawn
@@ -158,6 +161,8 @@ WORKLOADS = {
                        a_std=1.0, b_std=0.02, row_scale_std=0.05),
     "moe8": Workload("moe8", 11, 2048, 28672, 4096, "kn", ("pair_swiglu", "store_bf16"),
                      a_std=1.0, b_std=0.02, batch=8),
+    "decode": Workload("decode", 12, 64, 28672, 4096, "kn", ("pair_swiglu", "store_bf16"),
+                       a_std=1.0, b_std=0.02),
 }
 
 BY_INDEX = {w.index: w for w in WORKLOADS.values()}

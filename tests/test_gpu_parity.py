@@ -369,7 +369,7 @@ def test_graph_capture_replay_matches_eager():
 # ------------------------------------------------------------ full-size workloads
 
 FULL = ["tiny", "swiglu", "fp8", "downproj", "backward", "swiglu2w", "fp8in", "dswiglu", "drmsnorm",
-        "rmsswiglu", "rmsglu"]
+        "rmsswiglu", "rmsglu", "decode"]
 
 
 @pytest.mark.parametrize("name", FULL)
