@@ -151,7 +151,7 @@ struct KernelParams {
   float* amax;
   float* row_out;
   float* col_out;
-  uint16_t* c;   // bf16 output (ragged-tail and direct stores)
+  uint16_t* c;   // bf16 output (plain stores of a ragged last 16-byte group)
   uint8_t* c8;   // e4m3 output (ragged-tail stores)
   int64_t ldc, ldc8;
   const uint16_t* aux;  // residual or pre-activation (direct loads)

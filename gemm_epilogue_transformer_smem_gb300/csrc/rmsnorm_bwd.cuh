@@ -1,7 +1,7 @@
 // rmsnorm_bwd.cuh -- the second pass of the RMSNorm backward.
 //
 // For y = x * S * w with S[m] = 1/sqrt(mean_n x^2 + eps) ("Lean4-TileLang
-// Tensor Program Superoptimizer", section 3 "RMSNorm") and upstream gradient
+// Tensor Program Superoptimizer", section 9 "RMSNorm") and upstream gradient
 // dy, the GEMM that produced dy already reduced r[m] = sum_n w dy x in its
 // epilogue (ROW_DOT; CODA's reductions on the output tile).  Every element of
 // dx needs its row's r, so the rest is one memory-bound pass:

@@ -553,7 +553,7 @@ int oracle_cols(const oracle_problem *p, const int64_t *cols, int64_t ncols,
 /* The gradient of y = x * S * w, S = (mean_n x^2 + eps)^(-1/2), written out:
  * dy/dx contributes S w dy directly and, through S, -x S^3 / N times
  * sum_n w dy x (dS/dx[n] = -S^3 x[n] / N).  "Lean4-TileLang Tensor Program
- * Superoptimizer", section 3 "RMSNorm" (the forward S and its row
+ * Superoptimizer", section 9 "RMSNorm" (the forward S and its row
  * broadcast), taken backward the way the CODA page's backward epilogues
  * pair an on-chip reduction with the output tile. */
 void oracle_rmsnorm_backward(int64_t M, int64_t N, const uint16_t *dy, int64_t ld_dy,
