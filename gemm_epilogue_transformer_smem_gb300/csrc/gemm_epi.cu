@@ -183,9 +183,10 @@ gemm_epi_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* b
   return GEMM_EPI_OK;
 }
 
+// Ops that write an output buffer: each may appear once per program.
 bool is_output_op(int c) {
   return c == GEMM_EPI_OP_AMAX || c == GEMM_EPI_OP_STORE_BF16 || c == GEMM_EPI_OP_STORE_E4M3 ||
-         c == GEMM_EPI_OP_ROW_RMS_RSQRT || c == GEMM_EPI_OP_COL_SUM;
+         c == GEMM_EPI_OP_ROW_RMS_RSQRT || c == GEMM_EPI_OP_ROW_DOT || c == GEMM_EPI_OP_COL_SUM;
 }
 
 bool is_pre_pair_op(int c) {

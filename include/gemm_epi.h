@@ -138,7 +138,10 @@ typedef enum gemm_epi_b_layout {
 /*
  * Epilogue primitives.  The program is applied per output element, in order,
  * to a running fp32 value y that starts as acc[m, n].  Element-wise ops
- * transform y; output ops record y and leave it unchanged.
+ * transform y; output ops (AMAX, STORE_BF16, STORE_E4M3, ROW_RMS_RSQRT,
+ * ROW_DOT, COL_SUM) record y and leave it unchanged, and each appears at
+ * most once per program (gemm_epi_create rejects a repeat with
+ * GEMM_EPI_ERR_INVALID_VALUE).
  */
 typedef enum gemm_epi_op_code {
     GEMM_EPI_OP_SCALE_ALPHA = 1,        /* y = alpha * y            (args.alpha)            */

@@ -149,6 +149,9 @@ def test_create_accepts_fp8_operands(lib, types):
     (dict(ldc=516), N.GEMM_EPI_ERR_MISALIGNED),
     (dict(program=("store_bf16", "store_e4m3"), ldc8=520), N.GEMM_EPI_ERR_MISALIGNED),
     (dict(program=("store_bf16", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("store_bf16", "row_dot", "row_dot"), ld_aux=512), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("store_bf16", "row_rms", "row_dot"), ld_aux=512), N.GEMM_EPI_ERR_INVALID_VALUE),
+    (dict(program=("col_sum", "col_sum")), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(program=("pair_swiglu", "pair_swiglu")), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(program=("pair_swiglu:3", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
     (dict(N_=511, program=("pair_swiglu", "store_bf16")), N.GEMM_EPI_ERR_INVALID_VALUE),
@@ -298,3 +301,35 @@ def test_binding_supplies_every_argument_a_workload_needs(lib, name):
 class FakeStream:
     """Stands in for a torch CUDA stream on a machine without a GPU."""
     cuda_stream = 0
+
+
+def test_rmsnorm_backward_checks_arguments_on_the_host(lib):
+    """gemm_epi_rmsnorm_backward validates every pointer and stride before it
+    touches the device, so these errors come back without a GPU."""
+    M, N_ = 8, 16
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256  # 16-byte aligned, never dereferenced on the host
+
+    def args(**kw):
+        a = N.gemm_epi_rmsnorm_bwd_args()
+        a.M, a.N = M, N_
+        a.dy, a.ld_dy, a.x, a.ld_x = base, N_, base, N_
+        a.s, a.r, a.dx, a.ld_dx = base, base, base, N_
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    cases = [
+        (dict(dy=None), N.GEMM_EPI_ERR_INVALID_VALUE),           # dy is NULL
+        (dict(dy=base + 2), N.GEMM_EPI_ERR_MISALIGNED),          # dy not 16-byte aligned
+        (dict(ld_x=N_ - 8), N.GEMM_EPI_ERR_INVALID_VALUE),       # row stride < N
+        (dict(ld_dx=N_ + 4), N.GEMM_EPI_ERR_MISALIGNED),         # stride not a multiple of 8
+        (dict(r=None), N.GEMM_EPI_ERR_INVALID_VALUE),            # dx needs r
+        (dict(s=base + 2), N.GEMM_EPI_ERR_MISALIGNED),           # fp32 vectors 4-byte aligned
+        (dict(dw=base + 2), N.GEMM_EPI_ERR_MISALIGNED),
+        (dict(M=-1), N.GEMM_EPI_ERR_INVALID_VALUE),
+    ]
+    for kw, status in cases:
+        a = args(**kw)
+        assert lib.gemm_epi_rmsnorm_backward(ctypes.byref(a), None) == status, kw
+    assert lib.gemm_epi_rmsnorm_backward(None, None) == N.GEMM_EPI_ERR_INVALID_VALUE
