@@ -46,3 +46,21 @@ def test_second_pass_bytes():
     # dy and x read, dx written (bf16); w, S, r read and dw written (fp32)
     assert bench.finish_bytes(w) == 3 * 16384 * 4096 * 2 + 4 * (2 * 4096 + 2 * 16384)
     assert bench.finish_bytes(w) / 1e6 == pytest.approx(402.8, abs=0.1)
+
+
+def test_fused_bytes_and_binding_roofline():
+    w = synth.WORKLOADS
+    # swiglu: A 8192 x 4096 and B 4096 x 28672 read, C 8192 x 14336 written (bf16)
+    assert bench.fused_bytes(w["swiglu"]) == (8192 * 4096 + 4096 * 28672 + 8192 * 14336) * 2
+    # e4m3 operands are one byte each; the outputs stay bf16 + e4m3
+    assert bench.fused_bytes(w["fp8in"]) == 2 * 8192 * 8192 + 8192 * 8192 * (2 + 1)
+    # batched: every problem's operands and outputs
+    assert bench.fused_bytes(w["moe8"]) == 8 * ((2048 * 4096 + 4096 * 28672) * 2 + 2048 * 14336 * 2)
+    # the prefill-sized GEMMs are tensor bound, the 64-token decode step HBM bound
+    for name in ("swiglu", "fp8", "downproj", "backward", "dswiglu", "moe8"):
+        wl = w[name]
+        peaks, _ = bench.load_peaks()
+        tf = float(peaks.get("bf16_tflops", bench.FALLBACK_PEAKS["bf16_tflops"]))
+        assert bench.roofline_seconds(wl) == pytest.approx(wl.flops / (tf * 1e12)), name
+    assert bench.roofline_seconds(w["decode"]) < bench.LATENCY_BOUND_SECONDS  # timed as a graph replay
+    assert bench.roofline_seconds(w["swiglu"]) > bench.LATENCY_BOUND_SECONDS
