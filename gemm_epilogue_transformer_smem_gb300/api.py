@@ -63,6 +63,45 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _bytes_after(t: torch.Tensor) -> int:
+    """Bytes of the tensor's storage from its first element to the end."""
+    return t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+
+
+def _expect(name: str, t: Optional[torch.Tensor], kind: str, rows: int, cols: int = 1, ld: int = 1,
+            batch: int = 1, batch_stride: int = 0) -> None:
+    """Checks one buffer before its pointer crosses the C ABI, which sees
+    neither dtype nor size: ``kind`` is "bf16", "f32" or "byte" (any 8-bit
+    type), and the storage must hold ``batch`` matrices of ``rows`` x ``cols``
+    elements at row stride ``ld`` and batch stride ``batch_stride``."""
+    if t is None:
+        return
+    ok = {"bf16": t.dtype == torch.bfloat16, "f32": t.dtype == torch.float32,
+          "byte": t.element_size() == 1}[kind]
+    if not ok:
+        raise TypeError("%s: expected a %s tensor, got %s" % (name, kind, t.dtype))
+    if batch <= 0 or rows <= 0 or cols <= 0:
+        return
+    need = ((batch - 1) * batch_stride + (rows - 1) * ld + cols) * t.element_size()
+    if need > _bytes_after(t):
+        raise ValueError("%s: %d bytes needed from its first element, the storage holds %d"
+                         % (name, need, _bytes_after(t)))
+
+
+def _width_at(program: Sequence[str], N_: int):
+    """Accumulator width each op sees: N before a pair op, N/2 after it, 2N
+    after dswiglu."""
+    w, out = N_, []
+    for spec in program:
+        name = spec.partition(":")[0]
+        out.append((name, w))
+        if name.startswith("pair_"):
+            w = N_ // 2
+        elif name == "dswiglu":
+            w = 2 * N_
+    return out
+
+
 # Operand element types (desc.a_type / b_type); 8-bit operands are passed as
 # uint8 (or torch float8) tensors of codes.
 OPERAND_TYPES = {"bf16": N.GEMM_EPI_TYPE_BF16, "e4m3": N.GEMM_EPI_TYPE_E4M3, "e5m2": N.GEMM_EPI_TYPE_E5M2}
@@ -150,7 +189,31 @@ class Plan:
         a.workspace = _ptr(workspace)
         a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         a.timeout_ms, a.debug_flags = int(timeout_ms), int(debug_flags)
+        self._check(A, B, B2, bias, row_scale, residual, preact, C, C8, amax, row_out, col_out,
+                    a_scale_inv, b_scale_inv, col_scale)
         return a
+
+    def _check(self, A, B, B2, bias, row_scale, residual, preact, C, C8, amax, row_out, col_out,
+               a_scale_inv, b_scale_inv, col_scale):
+        d, M, K, Bt = self.desc, self.M, self.K, self.batch
+        op_kind = lambda t: "bf16" if t == "bf16" else "byte"  # noqa: E731
+        b_cols = self.N // 2 if self.dual else self.N
+        b_rows, b_inner = (K, b_cols) if self.b_layout == "kn" else (b_cols, K)
+        _expect("A", A, op_kind(self.a_type), M, K, d.lda, Bt, d.batch_stride_a)
+        _expect("B", B, op_kind(self.b_type), b_rows, b_inner, d.ldb, Bt, d.batch_stride_b)
+        _expect("B2", B2, op_kind(self.b_type), b_rows, b_inner, d.ldb, Bt, d.batch_stride_b)
+        _expect("C", C, "bf16", M, self.n_out, d.ldc, Bt, d.batch_stride_c)
+        _expect("C8", C8, "byte", M, self.n_out, d.ldc8, Bt, d.batch_stride_c8)
+        for name, t in (("residual", residual), ("preact", preact)):
+            _expect(name, t, "bf16", M, self.n_out, d.ld_aux, Bt, d.batch_stride_aux)
+        _expect("row_scale", row_scale, "f32", Bt * M)
+        _expect("row_out", row_out, "f32", Bt * M)
+        _expect("col_out", col_out, "f32", Bt * self.n_out)
+        for name, t in (("amax", amax), ("a_scale_inv", a_scale_inv), ("b_scale_inv", b_scale_inv)):
+            _expect(name, t, "f32", 1)
+        widths = dict((op, w) for op, w in _width_at(self.program, self.N))
+        _expect("bias", bias, "f32", widths.get("bias", 1))
+        _expect("col_scale", col_scale, "f32", widths.get("col_scale", 1))
 
     def run(self, *tensors, stream: Optional[torch.cuda.Stream] = None, **kw):
         """gemm_epi_run on the current (or given) CUDA stream; asynchronous."""
@@ -160,6 +223,7 @@ class Plan:
 
     def run_unfused(self, *tensors, scratch: torch.Tensor, stream=None, **kw):
         a = self.args(*tensors, **kw)
+        _expect("scratch", scratch, "bf16", self.M, self.N, scratch.stride(0))
         s = (stream or torch.cuda.current_stream()).cuda_stream
         N.check(self.lib.gemm_epi_run_unfused(self.handle, ctypes.byref(a), ctypes.c_void_p(scratch.data_ptr()),
                                               scratch.stride(0), ctypes.c_void_p(s)), self.lib)
@@ -222,6 +286,10 @@ def rmsnorm_backward(dy, x, s, r, *, w=None, add=None, dx=None, dw=None, stream=
     lib = N.load()
     a = N.gemm_epi_rmsnorm_bwd_args()
     a.M, a.N = dy.shape
+    for name, t in (("dy", dy), ("x", x), ("add", add), ("dx", dx)):
+        _expect(name, t, "bf16", a.M, a.N, 1 if t is None else t.stride(0))
+    for name, t, n in (("s", s, a.M), ("r", r, a.M), ("w", w, a.N), ("dw", dw, a.N)):
+        _expect(name, t, "f32", n)
     a.dy, a.ld_dy = _ptr(dy), dy.stride(0)
     a.x, a.ld_x = _ptr(x), x.stride(0)
     a.add, a.ld_add = _ptr(add), (add.stride(0) if add is not None else 0)

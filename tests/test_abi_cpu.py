@@ -333,3 +333,56 @@ def test_rmsnorm_backward_checks_arguments_on_the_host(lib):
         a = args(**kw)
         assert lib.gemm_epi_rmsnorm_backward(ctypes.byref(a), None) == status, kw
     assert lib.gemm_epi_rmsnorm_backward(None, None) == N.GEMM_EPI_ERR_INVALID_VALUE
+
+
+def test_binding_checks_dtypes_and_extents(lib):
+    """The C ABI sees only pointers, so the binding checks each tensor's
+    dtype and that its storage covers the declared extent before the call."""
+    import torch
+    M, N_, K = 64, 256, 128
+    plan = api.Plan(M, N_, K, ["bias", "pair_swiglu", "store_bf16", "amax"])
+    A = torch.zeros(M, K, dtype=torch.bfloat16)
+    B = torch.zeros(K, N_, dtype=torch.bfloat16)
+    C = torch.zeros(M, N_ // 2, dtype=torch.bfloat16)
+    amax = torch.zeros(1)
+    bias = torch.zeros(N_)  # before the pair op: N values
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8)
+    ok = dict(bias=bias, C=C, amax=amax, workspace=ws)
+    plan.args(A, B, **ok)
+    with pytest.raises(TypeError, match="A: expected a bf16"):
+        plan.args(A.float(), B, **ok)
+    with pytest.raises(TypeError, match="amax"):
+        plan.args(A, B, **dict(ok, amax=torch.zeros(1, dtype=torch.float64)))
+    with pytest.raises(ValueError, match="C: "):
+        plan.args(A, B, **dict(ok, C=C[1:]))          # one row short
+    with pytest.raises(ValueError, match="B: "):
+        plan.args(A, B.reshape(-1)[: K * N_ - 1].clone(), **ok)  # one element short
+    plan.args(A, B.reshape(-1).clone(), **ok)        # any shape whose storage covers K x N
+    plan.args(A, B[:, :8], **ok)                     # a view: its storage covers K x N
+    with pytest.raises(ValueError, match="bias"):
+        plan.args(A, B, **dict(ok, bias=bias[: N_ // 2].clone()))
+    # 8-bit operands accept any one-byte dtype; batched extents count every problem
+    p8 = api.Plan(M, N_, K, ["store_bf16"], b_layout="nk", a_type="e4m3", b_type="e4m3", batch=3,
+                  batch_stride_b=0)
+    A8, B8 = torch.zeros(3, M, K, dtype=torch.uint8), torch.zeros(N_, K, dtype=torch.float8_e4m3fn)
+    C3 = torch.zeros(3, M, N_, dtype=torch.bfloat16)
+    p8.args(A8, B8, C=C3, workspace=ws)
+    with pytest.raises(ValueError, match="A: "):
+        p8.args(A8[:2].clone(), B8, C=C3, workspace=ws)
+    with pytest.raises(TypeError, match="B: expected a byte"):
+        p8.args(A8, B8.to(torch.bfloat16), C=C3, workspace=ws)
+
+
+def test_rmsnorm_backward_binding_checks(lib):
+    import torch
+    M, N_ = 16, 64
+    dy, x = torch.zeros(M, N_, dtype=torch.bfloat16), torch.zeros(M, N_, dtype=torch.bfloat16)
+    s, r = torch.ones(M), torch.ones(M)
+    with pytest.raises(TypeError, match="dy"):
+        api.rmsnorm_backward(dy.float(), x, s, r, dx=x)
+    with pytest.raises(TypeError, match="r: "):
+        api.rmsnorm_backward(dy, x, s, r.double(), dx=x)
+    with pytest.raises(ValueError, match="w: "):
+        api.rmsnorm_backward(dy, x, s, r, w=torch.ones(N_ - 1), dx=x)
+    with pytest.raises(ValueError, match="dx: "):
+        api.rmsnorm_backward(dy, x, s, r, dx=x[1:].reshape(M - 1, N_))
