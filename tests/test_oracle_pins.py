@@ -243,6 +243,8 @@ def brute_force(A, B, b_is_nk, program, alpha=1.0, bias=None, row_scale=None, au
                     out["amax"] = max(out["amax"], abs(y))
                 elif op == "col_sum":
                     out["col"][j] += y
+                elif op.startswith("row_rms_unrounded"):
+                    out["row"][m] += y * y  # the fp64 value itself
                 elif op.startswith("row_rms"):
                     out["row"][m] += f64(bf16_bits_from_f32(np.array([y])))[0] ** 2
                 elif op == "store_e4m3":
@@ -260,6 +262,8 @@ PROGRAMS = [
     (("alpha", "bias", "pair_swiglu", "store_bf16"), "kn"),
     (("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"), "kn"),
     (("residual", "store_bf16", "row_rms:1e-6"), "kn"),
+    (("residual", "store_bf16", "row_rms_unrounded:1e-6"), "kn"),
+    (("alpha", "bias", "gelu_tanh", "store_bf16", "row_rms_unrounded:1e-3"), "nk"),
     (("gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
     (("row_scale", "silu", "store_bf16"), "nk"),
     (("row_scale", "pair_mul", "store_bf16"), "kn"),
@@ -295,8 +299,10 @@ def test_oracle_matches_brute_force(program, layout):
         cs = p.cols(list(range(nout)))
         np.testing.assert_allclose(cs["col_stat"], ref["col"], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(cs["y"], got["y"], rtol=1e-15, atol=0)
-    if any(op.startswith("row_rms") for op in program):
-        want = 1.0 / np.sqrt(ref["row"] / nout + 1e-6)
+    rms = [op for op in program if op.startswith("row_rms")]
+    if rms:
+        eps = float(rms[0].split(":")[1])
+        want = 1.0 / np.sqrt(ref["row"] / nout + eps)
         np.testing.assert_allclose(got["row_stat"], want, rtol=1e-12)
 
 
@@ -343,6 +349,50 @@ def test_row_rms_constant_rows_closed_form():
     res = bf16_bits_from_f32(np.repeat(c[:, None], N, 1))
     r = Problem(A, B, ["residual", "store_bf16", "row_rms:1e-6"], residual=res).rows()["row_stat"]
     np.testing.assert_allclose(r, 1 / np.sqrt(c * c + 1e-6), rtol=1e-15)
+
+
+def _rms_rows(mode):
+    """Rows whose epilogue value is 1 + 2^-10 in every column (B = 1, residual
+    2^-10, A = I): exactly representable in fp64, but not in bf16, where it
+    rounds to 1.  The two row-RMS modes must see different values."""
+    M, N = 3, 24
+    A = bf16_bits_from_f32(np.eye(M, 4))
+    B = bf16_bits_from_f32(np.ones((4, N)))
+    res = bf16_bits_from_f32(np.full((M, N), 2.0 ** -10))
+    return Problem(A, B, ["residual", "store_bf16", mode + ":1e-6"], residual=res).rows()["row_stat"]
+
+
+def test_row_rms_unrounded_closed_form():
+    """row_rms_unrounded: S = 1/sqrt(mean(y^2) + eps) of the fp64 value
+    ("Lean4-TileLang Tensor Program Superoptimizer", section 9, RMSNorm's S),
+    here mean(y^2) = (1 + 2^-10)^2 in closed form; row_rms squares the bf16
+    rounding of y, 1.0.  The pair differs by about 2^-10 relative, so squaring
+    the rounded value in the unrounded mode (or the reverse) fails here."""
+    y = 1.0 + 2.0 ** -10
+    unrounded = _rms_rows("row_rms_unrounded")
+    rounded = _rms_rows("row_rms")
+    np.testing.assert_allclose(unrounded, 1.0 / math.sqrt(y * y + 1e-6), rtol=1e-15)
+    np.testing.assert_allclose(rounded, 1.0 / math.sqrt(1.0 + 1e-6), rtol=1e-15)
+    assert np.all(np.abs(unrounded / rounded - 1.0) > 5e-4)
+
+
+def test_row_rms_unrounded_pure_python_mean():
+    """A random row: the unrounded mode's statistic equals a pure-Python
+    mean of the squared fp64 values the oracle reports, and differs from the
+    mean of their bf16 roundings."""
+    M, N, K = 4, 40, 12
+    A = rand_bf16((M, K), 0.5)
+    B = rand_bf16((K, N), 0.5)
+    res = rand_bf16((M, N))
+    p = Problem(A, B, ["residual", "store_bf16", "row_rms_unrounded:1e-6"], residual=res)
+    out = p.rows()
+    for m in range(M):
+        ys = [float(v) for v in out["y"][m]]
+        want = 1.0 / math.sqrt(sum(v * v for v in ys) / N + 1e-6)
+        assert out["row_stat"][m] == pytest.approx(want, rel=1e-13)
+        rounded = f64(bf16_bits_from_f32(np.array(ys)))
+        wrong = 1.0 / math.sqrt(float(np.sum(rounded * rounded)) / N + 1e-6)
+        assert abs(out["row_stat"][m] / wrong - 1.0) > 1e-6  # rounding changes this row
 
 
 def test_amax_and_stores_consistent():
