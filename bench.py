@@ -17,6 +17,7 @@ buffers, and the CPU oracle timed on a bounded sample.
 from __future__ import annotations
 
 import argparse
+import gc
 import glob
 import hashlib
 import json
@@ -52,7 +53,25 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip bare / unfused comparison runs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--per-config", default=None,
+                    help="comma-separated workloads measured after the headline, each at full size with its "
+                         "bare and unfused comparison (default: fp8,downproj,backward with the swiglu headline, "
+                         "none otherwise; 'none' to skip)")
     return ap.parse_args()
+
+
+# The benchmark configurations measured beside the SwiGLU headline: the FP8-
+# training epilogue, the down-projection with residual and row RMS, and the
+# GELU backward with column sums.
+DEFAULT_PER_CONFIG = ("fp8", "downproj", "backward")
+
+
+def per_config_names(args):
+    if args.per_config is None:
+        return list(DEFAULT_PER_CONFIG) if args.workload == "swiglu" else []
+    if args.per_config.strip().lower() in ("", "none"):
+        return []
+    return [n.strip() for n in args.per_config.split(",") if n.strip()]
 
 
 # ------------------------------------------------------------------ helpers
@@ -312,7 +331,7 @@ def time_steps(fn, steps, stream):
 def run_ours(args, world, rank, local):
     import torch
 
-    from gemm_epilogue_transformer_smem_gb300 import api, build, native, synth
+    from gemm_epilogue_transformer_smem_gb300 import api, build, synth
 
     build.build()
     dev = torch.device("cuda", local)
@@ -322,9 +341,9 @@ def run_ours(args, world, rank, local):
     plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
     out = api.allocate_outputs(plan, dev)
     stream = torch.cuda.current_stream(dev)
-    scales = dict(a_scale_inv=inp.a_scale_inv, b_scale_inv=inp.b_scale_inv)
     kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2,
-              col_scale=inp.col_scale, row_scale=inp.row_scale, **scales)
+              col_scale=inp.col_scale, row_scale=inp.row_scale, a_scale_inv=inp.a_scale_inv,
+              b_scale_inv=inp.b_scale_inv)
     fin = make_finish(w, inp, out, dev)
     launches_per_step = 2 if fin else 1
 
@@ -385,61 +404,134 @@ def run_ours(args, world, rank, local):
 
     extras = {}
     if not args.no_extras:
-        # Fused, bare GEMM (same main loop, store-only program) and unfused
-        # (bare GEMM + separate epilogue pass) timed in interleaved rounds so
-        # that all three see the same clock and power state; medians.
-        bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
-        bare_out = api.allocate_outputs(bare, dev)
-
-        def bare_step():
-            bare.run(inp.A, inp.B, C=bare_out.C, workspace=bare_out.workspace, B2=inp.B2, **scales)
-
-        scratch = bare_out.C
-
-        def unfused_step():
-            api.run_program(plan, inp.A, inp.B, out, unfused_scratch=scratch, **kw)
-            if fin:
-                fin()
-
-        fns = [("fused", step), ("bare", bare_step), ("unfused", unfused_step)]
-        try:
-            unfused_step()
-        except native.GemmEpiError:  # a program the separate pass does not cover
-            fns = fns[:2]
-        for _, f in fns[1:]:
-            for _ in range(3):
-                f()
-        n = max(3, min(args.steps // 4, 10))
-        t = {name: [] for name, _ in fns}
-        rng = random.Random(0)
-        for _ in range(15):
-            rng.shuffle(fns)  # no variant keeps a fixed place in the power-cap cycle
-            for name, fn in fns:
-                t[name].append(time_steps(fn, n, stream) / n)
-        med = {k: statistics.median(v) for k, v in t.items()}
-        # The floor of any two-pass design: the bare GEMM plus a separate
-        # pass (and the second pass, where the step has one) moving only
-        # its algorithmic bytes at the measured HBM copy bandwidth.
-        hbm_gbs = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        ideal = med["bare"] + (separate_pass_bytes(w) + (finish_bytes(w) if fin else 0)) / (hbm_gbs * 1e9)
-        extras = {
-            "bare_gemm_ms": med["bare"] * 1e3, "bare_gemm_tflops": flops / med["bare"] / 1e12,
-            "unfused_ideal_ms": ideal * 1e3, "fused_vs_unfused_ideal": ideal / med["fused"],
-            "unfused_ms": med["unfused"] * 1e3 if "unfused" in med else None,
-            "unfused_tflops": flops / med["unfused"] / 1e12 if "unfused" in med else None,
-            "fused_ms_interleaved": med["fused"] * 1e3,
-            "overhead_vs_bare": med["fused"] / med["bare"] - 1.0,
-            "comparison": "15 rounds of %d launches each, order shuffled per round, medians" % n,
-        }
-        del bare_out, scratch
+        extras = compare_variants(w, plan, inp, out, kw, fin, step, dev, stream, args.steps)
 
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(plan, w, inp, out, kw, dev, max(3, min(args.steps, 20)), world, fin)
 
+    l2_note = "no flush: inputs + output (%d MB) exceed the 129 MB L2" % (
+        sum(t.numel() * t.element_size() for t in (inp.A, inp.B, inp.B2, inp.aux, inp.bias)
+            if t is not None) // 2 ** 20 + plan.M * plan.n_out * 2 // 2 ** 20)
+    has_fin = fin is not None
+    per_config = {}
+    names = per_config_names(args)
+    if names:
+        # The headline's buffers are released first: each configuration
+        # allocates its own full-size inputs and outputs.
+        del inp, out, plan, kw, fin, gemm, step
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        for name in names:
+            per_config[name] = measure_config(name, args, dev, stream, local, world, rank)
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return
     peaks, src = load_peaks()
+    roofline = roofline_entry(w, fused_tflops)
+    second_pass = None
+    if has_fin:
+        # The memory-bound second pass, against the measured copy bandwidth
+        # (its time includes the clearing of dw that precedes each launch).
+        t_fin = fin_seconds / args.steps
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        nbytes = finish_bytes(w)
+        second_pass = {"kernel": "rmsnorm_bwd_kernel", "bound": "hbm", "us_per_launch": t_fin * 1e6,
+                       "achieved": nbytes / t_fin / 1e9, "peak": hbm, "unit": "GB/s",
+                       "frac": nbytes / t_fin / 1e9 / hbm, "algorithmic_bytes_per_launch": nbytes,
+                       "traffic": profiled_traffic(w.name + ":second_pass"),
+                       "peak_source": "%s HBM copy" % src}
+    cpu = None
+    if not args.no_cpu and world == 1:  # the oracle baseline is timed at N = 1 only
+        host = synth.make_inputs(w, "cpu")
+        tf, rows, threads, dt = oracle_rows_sample(w, host, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d rows%s x all %d output columns, K=%d (%.1f s)" % (
+                   rows, w.M, " of the first of %d problems" % w.batch if w.batch > 1 else "", w.n_out, w.K, dt)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.in_type == "bf16" else w.in_type,
+        "data": "synthetic",
+        "timing": "CUDA-graph replay of the %d steps" % args.steps if graph is not None else "stream launches",
+        "us_per_step": seconds / args.steps * 1e6,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "b_layout": w.b_layout,
+                   "program": list(w.program), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": l2_note},
+        "roofline": roofline,
+        **({"second_pass": second_pass} if second_pass else {}),
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+        **extras,
+    }
+    if per_config:
+        line["per_config"] = per_config
+    print(json.dumps(line), flush=True)
+
+
+def compare_variants(w, plan, inp, out, kw, fin, step, dev, stream, steps):
+    """Fused, bare GEMM (same main loop, store-only program) and unfused (bare
+    GEMM + separate epilogue pass) timed in interleaved rounds so that all
+    three see the same clock and power state; medians."""
+    from gemm_epilogue_transformer_smem_gb300 import api, native
+    types = dict(a_type=w.in_type, b_type=w.in_type)
+    scales = dict(a_scale_inv=kw.get("a_scale_inv"), b_scale_inv=kw.get("b_scale_inv"))
+    flops = float(w.flops)
+    bare = api.Plan(w.M, w.N, w.K, ["store_bf16"], b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
+    bare_out = api.allocate_outputs(bare, dev)
+
+    def bare_step():
+        bare.run(inp.A, inp.B, C=bare_out.C, workspace=bare_out.workspace, B2=inp.B2, **scales)
+
+    scratch = bare_out.C
+
+    def unfused_step():
+        api.run_program(plan, inp.A, inp.B, out, unfused_scratch=scratch, **kw)
+        if fin:
+            fin()
+
+    fns = [("fused", step), ("bare", bare_step), ("unfused", unfused_step)]
+    try:
+        unfused_step()
+    except native.GemmEpiError:  # a program the separate pass does not cover
+        fns = fns[:2]
+    for _, f in fns[1:]:
+        for _ in range(3):
+            f()
+    n = max(3, min(steps // 4, 10))
+    t = {name: [] for name, _ in fns}
+    rng = random.Random(0)
+    for _ in range(15):
+        rng.shuffle(fns)  # no variant keeps a fixed place in the power-cap cycle
+        for name, fn in fns:
+            t[name].append(time_steps(fn, n, stream) / n)
+    med = {k: statistics.median(v) for k, v in t.items()}
+    # The floor of any two-pass design: the bare GEMM plus a separate pass
+    # (and the second pass, where the step has one) moving only its
+    # algorithmic bytes at the measured HBM copy bandwidth.
+    hbm_gbs = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ideal = med["bare"] + (separate_pass_bytes(w) + (finish_bytes(w) if fin else 0)) / (hbm_gbs * 1e9)
+    return {
+        "bare_gemm_ms": med["bare"] * 1e3, "bare_gemm_tflops": flops / med["bare"] / 1e12,
+        "unfused_ideal_ms": ideal * 1e3, "fused_vs_unfused_ideal": ideal / med["fused"],
+        "unfused_ms": med["unfused"] * 1e3 if "unfused" in med else None,
+        "unfused_tflops": flops / med["unfused"] / 1e12 if "unfused" in med else None,
+        "fused_ms_interleaved": med["fused"] * 1e3,
+        "overhead_vs_bare": med["fused"] / med["bare"] - 1.0,
+        "comparison": "15 rounds of %d launches each, order shuffled per round, medians" % n,
+    }
+
+
+def roofline_entry(w, fused_tflops):
+    """The roofline object of one fused launch: tensor bound against the
+    measured bf16 burst peak (x 2 for 8-bit operands), or HBM bound against
+    the measured copy bandwidth when the operand bytes take longer."""
+    peaks, src = load_peaks()
+    flops = float(w.flops)
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_source = "%s burst bf16 (cuBLAS)" % src
     if w.in_type != "bf16":
@@ -467,46 +559,68 @@ def run_ours(args, world, rank, local):
         # (a seconds-long loop), the regime long timed regions run in.
         sustained = float(peaks["bf16_tflops_sustained"]) * (2.0 if w.in_type != "bf16" else 1.0)
         roofline["frac_of_sustained"] = fused_tflops / sustained
-    second_pass = None
+    return roofline
+
+
+def measure_config(name, args, dev, stream, local, world, rank):
+    """One more benchmark configuration at full size, measured the way the
+    headline is: a burst of fused launches with CUDA events, then the
+    interleaved fused / bare / unfused rounds, with the clocks sampled over
+    both.  Returns the config's entry of the line's per_config object."""
+    import torch
+    from gemm_epilogue_transformer_smem_gb300 import api, synth
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w, dev)
+    types = dict(a_type=w.in_type, b_type=w.in_type)
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, dual=w.dual, batch=w.batch, **types)
+    out = api.allocate_outputs(plan, dev)
+    kw = dict(alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias, aux=inp.aux, B2=inp.B2,
+              col_scale=inp.col_scale, row_scale=inp.row_scale, a_scale_inv=inp.a_scale_inv,
+              b_scale_inv=inp.b_scale_inv)
+    fin = make_finish(w, inp, out, dev)
+
+    def gemm():
+        api.run_program(plan, inp.A, inp.B, out, **kw)
+
+    def step():
+        gemm()
+        if fin:
+            fin()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = plan.query_status(out.workspace)
+    if status != 0:
+        raise RuntimeError("fused kernel reported status %d on %s" % (status, name))
+    steps = max(20, min(args.steps, 100))
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("begin")
     if fin:
-        # The memory-bound second pass, against the measured copy bandwidth
-        # (its time includes the clearing of dw that precedes each launch).
-        t_fin = fin_seconds / args.steps
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        nbytes = finish_bytes(w)
-        second_pass = {"kernel": "rmsnorm_bwd_kernel", "bound": "hbm", "us_per_launch": t_fin * 1e6,
-                       "achieved": nbytes / t_fin / 1e9, "peak": hbm, "unit": "GB/s",
-                       "frac": nbytes / t_fin / 1e9 / hbm, "algorithmic_bytes_per_launch": nbytes,
-                       "traffic": profiled_traffic(w.name + ":second_pass"),
-                       "peak_source": "%s HBM copy" % src}
-    cpu = None
-    if not args.no_cpu and world == 1:  # the oracle baseline is timed at N = 1 only
-        host = synth.make_inputs(w, "cpu")
-        tf, rows, threads, dt = oracle_rows_sample(w, host, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": "%d of %d rows%s x all %d output columns, K=%d (%.1f s)" % (
-                   rows, w.M, " of the first of %d problems" % w.batch if w.batch > 1 else "", w.n_out, w.K, dt)}
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.in_type == "bf16" else w.in_type,
-        "data": "synthetic",
-        "timing": "CUDA-graph replay of the %d steps" % args.steps if graph is not None else "stream launches",
-        "us_per_step": seconds / args.steps * 1e6,
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "b_layout": w.b_layout,
-                   "program": list(w.program), "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "no flush: inputs + output (%d MB) exceed the 129 MB L2" % (
-                       sum(t.numel() * t.element_size() for t in (inp.A, inp.B, inp.B2, inp.aux, inp.bias)
-                           if t is not None) // 2 ** 20 + plan.M * plan.n_out * 2 // 2 ** 20)},
-        "roofline": roofline,
-        **({"second_pass": second_pass} if second_pass else {}),
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk,
-        **extras,
-    }
-    print(json.dumps(line), flush=True)
+        seconds, gemm_seconds, _ = time_steps_split(gemm, fin, steps, stream)
+    else:
+        seconds = gemm_seconds = time_steps(step, steps, stream)
+    seconds = max_over_ranks(seconds, world)
+    gemm_seconds = max_over_ranks(gemm_seconds, world)
+    fused_tflops = float(w.flops) / (gemm_seconds / steps) / 1e12
+    extras = {} if args.no_extras else compare_variants(w, plan, inp, out, kw, fin, step, dev, stream, steps)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    clk = clocks.stop() if rank == 0 else None
+    entry = {"M": w.M, "N": w.N, "K": w.K, "program": list(w.program), "b_layout": w.b_layout,
+             "steps": steps, "ms_per_step": seconds / steps * 1e3,
+             "value": aggregate_value(float(w.flops) * steps, world, seconds) / 1e12,
+             "fused_tflops": fused_tflops, "roofline": roofline_entry(w, fused_tflops), "clocks": clk}
+    if fin:
+        entry["gemm_ms"] = gemm_seconds / steps * 1e3
+    entry.update(extras)
+    del inp, out, plan
+    return entry
 
 
 def roofline_seconds(w):

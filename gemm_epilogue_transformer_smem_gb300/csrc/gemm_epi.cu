@@ -776,12 +776,17 @@ gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args* ar
   int dev_id = 0;
   gemm_epi_status s = device_state(&dev, &dev_id);
   if (s) return s;
-  if (h->ws_bytes > GEMM_EPI_NO_ALLOC_SCRATCH_BYTES)
+  if (h->ws_bytes > GEMM_EPI_NO_ALLOC_SCRATCH_BYTES) {
+    // One 4-byte counter per 128-row block, M rounded up to 256 rows, per batch.
+    const int64_t counters = static_cast<int64_t>((GEMM_EPI_NO_ALLOC_SCRATCH_BYTES - WS_HEADER) / 4);
+    const int64_t max_m = counters / (2 * h->batch) * 2 * ge::BLOCK_M;
     return fail(GEMM_EPI_ERR_WORKSPACE,
                 "this plan needs %zu bytes of scratch; the built-in scratch of gemm_epi_run_no_alloc "
-                "holds %d (M is limited to %d rows)",
-                h->ws_bytes, GEMM_EPI_NO_ALLOC_SCRATCH_BYTES,
-                static_cast<int>((GEMM_EPI_NO_ALLOC_SCRATCH_BYTES - WS_HEADER) / 4 * ge::BLOCK_M));
+                "holds %d: %lld row-block counters, ceil(M/256)*2*batch of them, so with batch %lld "
+                "M is limited to %lld rows",
+                h->ws_bytes, GEMM_EPI_NO_ALLOC_SCRATCH_BYTES, static_cast<long long>(counters),
+                static_cast<long long>(h->batch), static_cast<long long>(max_m));
+  }
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);

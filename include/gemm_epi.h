@@ -297,8 +297,11 @@ GEMM_EPI_API gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_
  *  - The scratch (status words and per-row-tile counters) is one static
  *    device array of GEMM_EPI_NO_ALLOC_SCRATCH_BYTES bytes inside the
  *    library; every GPU that loads the library keeps it until the process
- *    exits.  Plans whose gemm_epi_workspace_size exceeds it (M above
- *    2,088,960 rows) are rejected with GEMM_EPI_ERR_WORKSPACE.
+ *    exits.  Plans whose gemm_epi_workspace_size exceeds it are rejected
+ *    with GEMM_EPI_ERR_WORKSPACE: after 256 bytes of status words it holds
+ *    16,320 row-block counters, and a plan needs ceil(M/256) * 2 * batch of
+ *    them (M up to 2,088,960 rows for one problem, a batch-th of that for a
+ *    batch).
  *  - The first call on a device looks up the array's address on that device
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
  *  - All calls share the array and clear it on their stream before the
@@ -310,8 +313,6 @@ GEMM_EPI_API gemm_epi_status gemm_epi_run_unfused(gemm_epi_handle h, const gemm_
 #define GEMM_EPI_NO_ALLOC_SCRATCH_BYTES 65536
 GEMM_EPI_API gemm_epi_status gemm_epi_run_no_alloc(gemm_epi_handle h, const gemm_epi_args *args, void *stream);
 
-/* Synchronises `stream`, then reads the status word the last run on that
- * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
 /*
  * RMSNorm backward, second pass.  For y = x * S * w (S[m] = 1/sqrt(mean_n
  * x^2 + eps), the forward's ROW_RMS_RSQRT output) and the upstream gradient
@@ -341,6 +342,8 @@ typedef struct gemm_epi_rmsnorm_bwd_args {
  * capture-safe; checks sizes, pointers and alignment first. */
 GEMM_EPI_API gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bwd_args *args, void *stream);
 
+/* Synchronises `stream`, then reads the status word the last run on that
+ * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
 GEMM_EPI_API gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
 
 /* Static description of a status code. */

@@ -64,3 +64,19 @@ def test_fused_bytes_and_binding_roofline():
         assert bench.roofline_seconds(wl) == pytest.approx(wl.flops / (tf * 1e12)), name
     assert bench.roofline_seconds(w["decode"]) < bench.LATENCY_BOUND_SECONDS  # timed as a graph replay
     assert bench.roofline_seconds(w["swiglu"]) > bench.LATENCY_BOUND_SECONDS
+
+
+def test_per_config_defaults_to_the_other_benchmark_configs():
+    """The default (SwiGLU) line also measures the FP8, down-projection and
+    backward configurations; other workloads measure none unless asked."""
+    class A:
+        workload, per_config = "swiglu", None
+    assert bench.per_config_names(A) == ["fp8", "downproj", "backward"]
+    A.workload = "fp8"
+    assert bench.per_config_names(A) == []
+    A.per_config = "backward, dswiglu"
+    assert bench.per_config_names(A) == ["backward", "dswiglu"]
+    A.per_config = "none"
+    assert bench.per_config_names(A) == []
+    for name in bench.DEFAULT_PER_CONFIG:
+        assert name in synth.WORKLOADS

@@ -13,7 +13,7 @@ import torch
 import oracle
 from gemm_epilogue_transformer_smem_gb300 import api, native, synth
 
-from parity import (bits, check_amax, check_bf16, check_cols, check_rows, compare_cols,
+from parity import (bits, check_amax, check_bf16, check_cols, check_e4m3, check_rows, compare_cols,
                     compare_rows, oracle_problem, run_cuda)
 
 pytestmark = pytest.mark.gpu
@@ -381,10 +381,10 @@ def test_full_size_sampled_parity(name):
     nrows = 96 if w.M > 128 else w.M
     rows = np.unique(np.concatenate([rng.choice(w.M, nrows, replace=False), [0, w.M - 1]]))
     p = oracle_problem(w, inp)
-    ref = compare_rows(w, inp, out, rows=rows, oracle_p=p)
+    ref = compare_rows(w, inp, out, rows=rows, oracle_p=p, report=name)
     ncols = 24 if w.n_out > 64 else w.n_out
     cols = np.unique(np.concatenate([rng.choice(w.n_out, ncols, replace=False), [0, w.n_out - 1]]))
-    compare_cols(w, inp, out, cols, oracle_p=p)
+    compare_cols(w, inp, out, cols, oracle_p=p, report=name)
     prog = [op.partition(":")[0] for op in w.program]
     # Invariants over the whole output.
     if "amax" in prog:
@@ -401,6 +401,62 @@ def test_full_size_sampled_parity(name):
         s = c.sum(0)
         bound = 2.0 ** -8 * c.abs().sum(0) + 1e-6
         assert torch.all((out.col_out.double() - s).abs() <= bound)
+
+
+def test_full_size_fp8_against_the_whole_oracle():
+    """The FP8-training workload (M = N = K = 8192: ReLU(0.5 A@B + bias),
+    AMAX, bf16 and e4m3 stores) against the fp64 oracle over every element,
+    in row blocks.  AMAX feeds the next FP8 quantisation (the cuDNN Graph API
+    tutorial's matmul epilogue), so the whole-tensor maximum is checked to one
+    bf16 ulp of the fp64 value, not only through invariants and samples."""
+    w = W["fp8"]
+    inp = synth.make_inputs(w, DEV)
+    plan, out = run_cuda(w, inp)
+    p = oracle_problem(w, inp)
+    amax = 0.0
+    c8_mismatch = 0
+    step = 1024
+    for r0 in range(0, w.M, step):
+        rows = list(range(r0, min(w.M, r0 + step)))
+        ref = p.rows(rows)
+        amax = max(amax, ref["amax"])
+        check_bf16(bits(out.C[r0:r0 + len(rows)]), ref["y"], "C rows %d.." % r0,
+                   report="fp8-full" if r0 == 0 else None)
+        c8_mismatch += check_e4m3(out.C8[r0:r0 + len(rows)].cpu().numpy(), ref["c_e4m3"], ref["y"] * inp.fp8_scale)
+        del ref
+    check_amax(float(out.amax.item()), amax)
+    print("fp8 whole-oracle: amax %r (oracle %r), e4m3 codes at a midpoint: %d" % (
+        float(out.amax.item()), amax, c8_mismatch))
+
+
+# The store path's chunk that straddles the output edge (columns 512..543)
+# and the chunks past it, in the static FP8 kernels (bf16 + e4m3 stores) and
+# the bf16-only backward kernel.  A race between a chunk's TMA store and a
+# later chunk's staging writes once left the straddling columns unwritten;
+# repeated runs guard against its return.
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+@pytest.mark.parametrize("name,N", [("fp8", 528), ("fp8", 536), ("backward", 520)])
+def test_edge_chunk_stores_repeated(name, N, variant):
+    w = small(name, 257 if name == "fp8" else 200, N, 264 if name == "fp8" else 192)
+    inp = synth.make_inputs(w, DEV)
+    cols = list(range(480, w.n_out))
+    p = oracle_problem(w, inp)
+    ref = p.cols(cols)
+    ref8 = p.rows()["c_e4m3"][:, cols] if "store_e4m3" in w.program else None
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout)
+    out = api.allocate_outputs(plan, DEV)
+    idx = torch.as_tensor(cols, device=DEV)
+    for it in range(50):
+        out.C.fill_(float("nan"))
+        if out.C8 is not None:
+            out.C8.fill_(0x7F)  # e4m3 NaN
+        api.run_program(plan, inp.A, inp.B, out, alpha=inp.alpha, fp8_scale=inp.fp8_scale, bias=inp.bias,
+                        aux=inp.aux, debug_flags=VARIANTS[variant])
+        torch.cuda.synchronize()
+        assert plan.query_status(out.workspace) == 0
+        check_bf16(bits(out.C[:, idx]), ref["y"], "run %d, C columns 480.." % it)
+        if ref8 is not None:
+            check_e4m3(out.C8[:, idx].cpu().numpy(), ref8, ref["y"] * inp.fp8_scale)
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
