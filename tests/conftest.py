@@ -32,7 +32,7 @@ def pytest_terminal_summary(terminalreporter):
     (the pass / fail bound is floored at 1% of the tensor RMS; the plain
     relative error and the count of elements above 2e-2 are listed here)."""
     parity = sys.modules.get("parity")
-    if parity is None or not getattr(parity, "REPORTS", None):
+    if parity is None or not (getattr(parity, "REPORTS", None) or getattr(parity, "NOTES", None)):
         return
     tr = terminalreporter
     tr.write_sep("-", "bf16 error vs the fp64 oracle (unfloored relative error; floored bound decides)")
@@ -40,3 +40,5 @@ def pytest_terminal_summary(terminalreporter):
         tr.write_line("%-10s %-10s n=%-9d max|g-r|/|r|=%.3g (|r|=%.2g)  >2e-2: %d  r==0: %d  max err/bound=%.3f" % (
             name, what, st["n"], st["max_rel_unfloored"], st["ref_at_max_rel"],
             st["n_above_2e-2_unfloored"], st["zeros_in_ref"], st["max_err_over_bound"]))
+    for note in getattr(parity, "NOTES", []):
+        tr.write_line(note)

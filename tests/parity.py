@@ -8,7 +8,10 @@ Tolerances (as the benchmark statement fixes them, with the readings noted):
   fp32 columns   |g - r| <= 1e-3 * sum_m |y[m, n]|
   AMAX           within one bf16 ulp of r
   e4m3 codes     identical, except two adjacent codes when the fp64 value lies
-                 within one bf16 ulp (2^-8 relative) of the midpoint between them
+                 within one bf16 ulp (2^-8 relative) of the midpoint between them,
+                 that ulp floored at 1% of the compared values' RMS like the
+                 bf16 bound (a value from a cancellation near zero carries the
+                 fp32 error of the tensor's scale, not of its own size)
 """
 from __future__ import annotations
 
@@ -32,6 +35,7 @@ def bits(t: torch.Tensor) -> np.ndarray:
 # of the pytest run (tests/conftest.py): the floored bound decides pass or
 # fail, the unfloored relative error is reported beside it.
 REPORTS = []
+NOTES = []  # one-line results printed beside them
 
 
 def bf16_error_stats(g: np.ndarray, ref: np.ndarray) -> dict:
@@ -79,6 +83,8 @@ def check_bf16(got_bits: np.ndarray, ref: np.ndarray, what="C", report=None):
 
 
 def check_e4m3(got: np.ndarray, want_codes: np.ndarray, ref_scaled: np.ndarray):
+    """Returns the number of codes that differ (each one adjacent to the
+    oracle's and at a rounding boundary within the tolerance)."""
     got = np.asarray(got, dtype=np.uint8)
     want = np.asarray(want_codes, dtype=np.uint8)
     assert got.shape == want.shape
@@ -86,6 +92,8 @@ def check_e4m3(got: np.ndarray, want_codes: np.ndarray, ref_scaled: np.ndarray):
     diff = (got != want) & ~(zero(got) & zero(want))
     if not diff.any():
         return 0
+    ref_scaled = np.asarray(ref_scaled, dtype=np.float64)
+    floor = 1e-2 * math.sqrt(float(np.mean(ref_scaled * ref_scaled)))
     for idx in np.argwhere(diff):
         i = tuple(idx)
         dg = float(oracle.e4m3_to_f64([got[i]])[0])
@@ -96,7 +104,7 @@ def check_e4m3(got: np.ndarray, want_codes: np.ndarray, ref_scaled: np.ndarray):
         between = oracle.to_e4m3([(lo + hi) / 2])[0]
         mid = (lo + hi) / 2
         adjacent = oracle.e4m3_to_f64([between])[0] in (lo, hi)
-        near = abs(r - mid) <= 2.0 ** -8 * max(abs(mid), 2.0 ** -9)
+        near = abs(r - mid) <= 2.0 ** -8 * max(abs(mid), floor, 2.0 ** -9)
         assert adjacent and near, "e4m3 code %s: got %#x want %#x for value %r" % (
             i, got[i], want[i], r)
     return int(diff.sum())

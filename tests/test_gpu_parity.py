@@ -13,7 +13,8 @@ import torch
 import oracle
 from gemm_epilogue_transformer_smem_gb300 import api, native, synth
 
-from parity import (bits, check_amax, check_bf16, check_cols, check_e4m3, check_rows, compare_cols,
+import parity
+from parity import (bf16_ulp, bits, check_amax, check_bf16, check_cols, check_e4m3, check_rows, compare_cols,
                     compare_rows, oracle_problem, run_cuda)
 
 pytestmark = pytest.mark.gpu
@@ -336,6 +337,13 @@ def test_bounded_wait_reports_timeout_and_context_survives(variant):
                     debug_flags=native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD | VARIANTS[variant])
     torch.cuda.synchronize()
     assert plan.query_status(out.workspace) == native.GEMM_EPI_ERR_TIMEOUT
+    # Status words: [0] bit 0 a wait ran out, bit 1 the drain of the operand
+    # loads after it also ran out; [3] the stages the drain settled.  On the
+    # CTA-pair kernel the even CTA skipped arming stage 0, into which the odd
+    # CTA still loaded: the drain arms it and waits for those bytes (bit 8).
+    words = out.workspace[:16].view(torch.int32).cpu().tolist()
+    assert words[0] & 1 and not words[0] & 2, words
+    assert words[3] == (0 if "1sm" in variant else 1 << 8), words
     # The context still works: a normal run afterwards is correct.
     api.run_program(plan, inp.A, inp.B, out, bias=inp.bias)
     torch.cuda.synchronize()
@@ -424,9 +432,10 @@ def test_full_size_fp8_against_the_whole_oracle():
                    report="fp8-full" if r0 == 0 else None)
         c8_mismatch += check_e4m3(out.C8[r0:r0 + len(rows)].cpu().numpy(), ref["c_e4m3"], ref["y"] * inp.fp8_scale)
         del ref
+    parity.NOTES.append("fp8 whole tensor vs oracle: amax %r (oracle %r, one bf16 ulp %.3g); e4m3 codes "
+                        "differing at a rounding boundary: %d of %d" % (
+                            float(out.amax.item()), amax, bf16_ulp(amax), c8_mismatch, w.M * w.n_out))
     check_amax(float(out.amax.item()), amax)
-    print("fp8 whole-oracle: amax %r (oracle %r), e4m3 codes at a midpoint: %d" % (
-        float(out.amax.item()), amax, c8_mismatch))
 
 
 # The store path's chunk that straddles the output edge (columns 512..543)
