@@ -37,7 +37,8 @@
 //
 // Every mbarrier wait is bounded: when one runs out the CTA records a status
 // in the workspace, raises a shared abort flag that every other wait checks,
-// waits (bounded) for its own copies and MMAs in flight, frees TMEM and exits.
+// waits (bounded) for its copies and MMAs in flight -- the operand loads of
+// both CTAs of a pair included -- frees TMEM and exits.
 #pragma once
 
 #include <stdint.h>
@@ -334,13 +335,70 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return wait_slow<CG>(bar, parity, abort_flag, p, where);
 }
 
-// Short bounded wait used while draining after an abort (no flag check).
-static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+// Short bounded wait used while draining after an abort (no flag check);
+// false when the limit ran out first.
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
 #pragma unroll 1
   while (!ptx::mbar_test(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > limit_ns) return;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
   }
+  return true;
+}
+
+// Operand loads issued into one stage: a 2-bit count per stage (mod 4).
+__device__ __forceinline__ uint32_t count_load(uint32_t cnt, uint32_t stage) {
+  const uint32_t sh = 2u * stage;
+  return (cnt & ~(3u << sh)) | ((((cnt >> sh) & 3u) + 1u) & 3u) << sh;
+}
+
+// After an abort: waits (bounded) until every operand load issued into this
+// CTA group's shared memory has landed, so that no copy writes into shared
+// memory after the group exits.  Runs in the CTA that owns the full
+// barriers (the even CTA of a pair), once every role of both CTAs is done.
+// `own` and `peer` hold the per-stage load counts of this CTA and of the odd
+// CTA, whose loads complete on this CTA's barriers.  The producers advance
+// in step (each waits on an empty barrier that the pair's MMA commit frees),
+// so per stage the counts differ by at most one:
+//   equal         the last phase holds both halves: wait for it;
+//   own = peer+1  this CTA armed a phase the odd CTA never loaded into:
+//                 count the missing half as arrived, then wait;
+//   peer = own+1  the odd CTA loaded into a phase this CTA never armed
+//                 (armed here now for both halves, this CTA's half counted
+//                 as arrived), then wait for the odd CTA's bytes.
+// Records status bit 1 when a wait ran out and, in status word 3, the stages
+// settled each way (bits 0-7 and 8-15).
+template <int CG, int STAGES>
+__device__ __noinline__ void drain_operand_loads(uint32_t bar_full0, uint32_t own, uint32_t peer,
+                                                 uint32_t half_bytes, uint32_t* status) {
+  bool late = false;
+  uint32_t settled = 0;
+#pragma unroll 1
+  for (uint32_t s = 0; s < STAGES; ++s) {
+    const uint32_t bar = bar_full0 + 8u * s;
+    uint32_t n = (own >> (2u * s)) & 3u;
+    if (CG == 2) {
+      const uint32_t np = (peer >> (2u * s)) & 3u;
+      const uint32_t d = (n - np) & 3u;
+      if (d == 1u) {
+        ptx::mbar_complete_tx(bar, half_bytes);
+        settled |= 1u << s;
+      } else if (d == 3u) {
+        ptx::mbar_arrive_expect_tx(bar, 2u * half_bytes);
+        ptx::mbar_complete_tx(bar, half_bytes);
+        settled |= 1u << (8u + s);
+        n = np;
+      } else if (d == 2u) {
+        late = true;  // not reachable when the producers keep in step
+        continue;
+      }
+    }
+    // The last phase this stage was loaded in has parity (n - 1) & 1; with no
+    // load at all that names the phase before the first, which tests complete.
+    if (!drain_wait(bar, (n + 1u) & 1u, DRAIN_LIMIT_NS)) late = true;
+  }
+  if (late) atomicOr(status, 2u);
+  if (settled) atomicOr(status + 3, settled);
 }
 
 // tcgen05 shared-memory descriptor for a 128B-swizzled operand tile.
@@ -578,8 +636,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
+  // misc[0] TMEM base, misc[1] abort flag, misc[2] the odd CTA's per-stage
+  // load counts (written there by the odd CTA of a pair).
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
+  uint32_t load_cnt = 0;  // producer lane: operand loads issued per stage (2 bits each)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -625,7 +686,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------- producer
     if (lane == 0 && p.num_k_blocks > 0) {
       uint32_t stage = 0, phase = 0;
-      uint32_t issued = 0, issued_parity = 0;  // per-stage bits, for the abort drain
       bool ok = true;
       for (int t = group; ok && t < p.num_tiles; t += num_groups) {
         int bt, mb, nb;
@@ -680,10 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * K_STEP, b_col, zb);
               }
             }
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          } else {
-            issued &= ~(1u << stage);
+            load_cnt = count_load(load_cnt, stage);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -691,12 +748,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok && rank == 0) {
-        // Loads still in flight land before the CTA exits.  (The odd CTA of a
-        // pair cannot observe its loads, which complete on the even CTA's
-        // barrier; the abort path waits out a fixed delay at the end.)
-        for (uint32_t s = 0; s < STAGES; ++s)
-          if (issued & (1u << s)) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, DRAIN_LIMIT_NS);
+      if (CG == 2 && rank == 1) {
+        // This CTA's loads complete on the even CTA's barriers: its counts go
+        // there for the abort drain (read after the cluster barrier below).
+        ptx::st_shared_cluster_u32(ptx::mapa_shared(sbase + L::OFF_MISC + 8u, 0), load_cnt);
       }
     }
   } else if (warp == 1) {
@@ -1117,15 +1172,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
-  if (threadIdx.x == 0 && *abort_flag) {
-    // After an abort, copies this CTA cannot observe (the odd CTA's operand
-    // loads) get a fixed 200 us to land before shared memory is released.
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (ptx::globaltimer_ns() - t0 < 200000ull) {
-    }
-  }
   __syncwarp();  // role branches reconverge before the warp-aligned barrier
   ptx::tc_fence_before_sync();
+  // Every role of the group has finished: any abort flag is set by now, and
+  // the odd CTA's load counts are visible to the even CTA.
+  if (CG == 2)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
+  if (threadIdx.x == 0 && rank == 0 && *abort_flag && p.num_k_blocks > 0)
+    drain_operand_loads<CG, STAGES>(bar(BAR_FULL), load_cnt, CG == 2 ? misc[2] : 0u,
+                                    A_STAGE_BYTES + L::B_STAGE_BYTES, p.status);
+  __syncwarp();
   if (CG == 2)
     ptx::cluster_sync();  // no CTA of the pair releases TMEM or smem the other still uses
   else

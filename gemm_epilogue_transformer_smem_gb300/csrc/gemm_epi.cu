@@ -885,7 +885,8 @@ gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void* workspace, 
   e = cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy of the status words");
   if (words[0] & 1u)
-    return fail(GEMM_EPI_ERR_TIMEOUT, "in-kernel wait ran out (site %u, block %u)", words[1], words[2]);
+    return fail(GEMM_EPI_ERR_TIMEOUT, "in-kernel wait ran out (site %u, block %u)%s", words[1], words[2],
+                (words[0] & 2u) ? "; waiting for its operand loads to land also ran out" : "");
   return GEMM_EPI_OK;
 }
 

@@ -452,8 +452,12 @@ def test_edge_chunk_stores_repeated(name, N, variant):
     p = oracle_problem(w, inp)
     ref = p.cols(cols)
     ref8 = p.rows()["c_e4m3"][:, cols] if "store_e4m3" in w.program else None
-    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout)
+    # e4m3 rows must start on 16-byte boundaries: a ragged e4m3 width gets a padded row stride
+    ldc8 = (w.n_out + 15) // 16 * 16
+    plan = api.Plan(w.M, w.N, w.K, w.program, b_layout=w.b_layout, ldc8=ldc8)
     out = api.allocate_outputs(plan, DEV)
+    if out.C8 is not None:
+        out.C8 = torch.empty((w.M, ldc8), dtype=torch.uint8, device=DEV)
     idx = torch.as_tensor(cols, device=DEV)
     for it in range(50):
         out.C.fill_(float("nan"))
