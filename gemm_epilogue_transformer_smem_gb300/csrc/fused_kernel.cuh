@@ -442,6 +442,51 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float x) {
 
 __device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
 
+// ---- pairs of values in sm_100's packed fp32 arithmetic (f32x2 add, mul,
+// fma: two lanes per instruction, each rounded like its scalar form); the
+// special-function steps (ex2, rcp) stay scalar.
+
+__device__ __forceinline__ float2 splat2(float c) { return make_float2(c, c); }
+
+// 1 / (1 + 2^zl) of two values: the sigmoid of z for zl = -z log2 e.
+__device__ __forceinline__ float2 sigmoid_from_neg_log2_f2(float2 zl) {
+  const float2 d = __fadd2_rn(make_float2(ptx::ex2_approx(zl.x), ptx::ex2_approx(zl.y)), splat2(1.0f));
+  return make_float2(ptx::rcp_approx(d.x), ptx::rcp_approx(d.y));
+}
+
+// sigmoid(2u) of GELU-tanh, 2u = x (GELU_K0 + GELU_K1 x^2), from x and x^2.
+__device__ __forceinline__ float2 gelu_sigmoid_f2(float2 x, float2 x2) {
+  const float2 zl = __fmul2_rn(x, __ffma2_rn(x2, splat2(-GELU_K1 * LOG2E), splat2(-GELU_K0 * LOG2E)));
+  return sigmoid_from_neg_log2_f2(zl);
+}
+
+__device__ __forceinline__ float2 gelu_tanh_f2(float2 x) {
+  return __fmul2_rn(x, gelu_sigmoid_f2(x, __fmul2_rn(x, x)));
+}
+
+// s + x s (1 - s) (2u)' of two values (the derivative above).
+__device__ __forceinline__ float2 gelu_tanh_grad_f2(float2 x) {
+  const float2 x2 = __fmul2_rn(x, x);
+  const float2 s = gelu_sigmoid_f2(x, x2);
+  const float2 t = __fmul2_rn(__fmul2_rn(x, s), __ffma2_rn(s, splat2(-1.0f), splat2(1.0f)));
+  return __ffma2_rn(t, __ffma2_rn(x2, splat2(3.0f * GELU_K1), splat2(GELU_K0)), s);
+}
+
+__device__ __forceinline__ float2 silu_f2(float2 x) {
+  return __fmul2_rn(x, sigmoid_from_neg_log2_f2(__fmul2_rn(x, splat2(-LOG2E))));
+}
+
+// v[2i], v[2i+1] <- f(pair i, i) for every pair of an even-length array.
+template <int NV, class F>
+__device__ __forceinline__ void for_pairs(float (&v)[NV], F&& f) {
+#pragma unroll
+  for (int i = 0; i < NV / 2; ++i) {
+    const float2 r = f(make_float2(v[2 * i], v[2 * i + 1]), i);
+    v[2 * i] = r.x;
+    v[2 * i + 1] = r.y;
+  }
+}
+
 __device__ __forceinline__ float bf16_round_f(float x) {
   const uint32_t h = ptx::pack_bf16x2(x, 0.0f) & 0xFFFFu;
   return __uint_as_float(h << 16);
@@ -454,21 +499,18 @@ template <int NV, class CodeT>
 __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], const KernelParams& p,
                                                 int col0, int ncols, float row_scale_m) {
   switch (static_cast<int>(code)) {
-    case GEMM_EPI_OP_SCALE_ALPHA:
-#pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] *= p.alpha;
+    case GEMM_EPI_OP_SCALE_ALPHA: {
+      const float2 a = splat2(p.alpha);
+      for_pairs(v, [&](float2 y, int) { return __fmul2_rn(y, a); });
       break;
+    }
     case GEMM_EPI_OP_ADD_BIAS_COL:
       if (col0 + NV <= ncols) {
         const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);
-#pragma unroll
-        for (int q = 0; q < NV / 4; ++q) {
-          const float4 b = __ldg(b4 + q);
-          v[4 * q + 0] += b.x;
-          v[4 * q + 1] += b.y;
-          v[4 * q + 2] += b.z;
-          v[4 * q + 3] += b.w;
-        }
+        for_pairs(v, [&](float2 y, int i) {
+          const float4 b = __ldg(b4 + i / 2);  // one 16-byte load per two pairs
+          return __fadd2_rn(y, (i & 1) ? make_float2(b.z, b.w) : make_float2(b.x, b.y));
+        });
       } else {
 #pragma unroll
         for (int j = 0; j < NV; ++j)
@@ -478,35 +520,30 @@ __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], cons
     case GEMM_EPI_OP_MUL_COL_SCALE:
       if (col0 + NV <= ncols) {
         const float4* c4 = reinterpret_cast<const float4*>(p.col_scale + col0);
-#pragma unroll
-        for (int q = 0; q < NV / 4; ++q) {
-          const float4 c = __ldg(c4 + q);
-          v[4 * q + 0] *= c.x;
-          v[4 * q + 1] *= c.y;
-          v[4 * q + 2] *= c.z;
-          v[4 * q + 3] *= c.w;
-        }
+        for_pairs(v, [&](float2 y, int i) {
+          const float4 c = __ldg(c4 + i / 2);
+          return __fmul2_rn(y, (i & 1) ? make_float2(c.z, c.w) : make_float2(c.x, c.y));
+        });
       } else {
 #pragma unroll
         for (int j = 0; j < NV; ++j)
           if (col0 + j < ncols) v[j] *= __ldg(p.col_scale + col0 + j);
       }
       break;
-    case GEMM_EPI_OP_MUL_ROW_SCALE:
-#pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] *= row_scale_m;
+    case GEMM_EPI_OP_MUL_ROW_SCALE: {
+      const float2 r = splat2(row_scale_m);
+      for_pairs(v, [&](float2 y, int) { return __fmul2_rn(y, r); });
       break;
+    }
     case GEMM_EPI_OP_ACT_GELU_TANH:
-#pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] = gelu_tanh_f(v[j]);
+      for_pairs(v, [&](float2 y, int) { return gelu_tanh_f2(y); });
       break;
     case GEMM_EPI_OP_ACT_RELU:
 #pragma unroll
       for (int j = 0; j < NV; ++j) v[j] = fmaxf(v[j], 0.0f);
       break;
     case GEMM_EPI_OP_ACT_SILU:
-#pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] = silu_f(v[j]);
+      for_pairs(v, [&](float2 y, int) { return silu_f2(y); });
       break;
     default:
       break;
@@ -518,9 +555,12 @@ __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], cons
 template <int G, bool SILU>
 __device__ __forceinline__ void pair_combine_g(const float (&a)[64], float (&out)[32]) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int gate = (j / G) * 2 * G + (j % G);
-    out[j] = (SILU ? silu_f(a[gate]) : a[gate]) * a[gate + G];
+  for (int j = 0; j < 32; j += 2) {  // outputs j and j + 1 as one packed pair
+    const int g0 = (j / G) * 2 * G + (j % G), g1 = ((j + 1) / G) * 2 * G + ((j + 1) % G);
+    const float2 gate = make_float2(a[g0], a[g1]), up = make_float2(a[g0 + G], a[g1 + G]);
+    const float2 r = __fmul2_rn(SILU ? silu_f2(gate) : gate, up);
+    out[j] = r.x;
+    out[j + 1] = r.y;
   }
 }
 
@@ -552,12 +592,20 @@ __device__ __forceinline__ void pair_combine(const float (&a)[64], float (&out)[
 template <int G>
 __device__ __forceinline__ void dswiglu_expand_g(const float (&dh)[16], const float (&x)[32], float (&out)[32]) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int gate = (j / G) * 2 * G + (j % G);
-    const float gt = x[gate], up = x[gate + G];
-    const float s = sigmoid_f(gt);
-    out[gate] = dh[j] * up * (s * fmaf(gt, 1.0f - s, 1.0f));
-    out[gate + G] = dh[j] * (gt * s);
+  for (int j = 0; j < 16; j += 2) {  // pairs j and j + 1 as one packed pair
+    const int g0 = (j / G) * 2 * G + (j % G), g1 = ((j + 1) / G) * 2 * G + ((j + 1) % G);
+    const float2 gt = make_float2(x[g0], x[g1]), up = make_float2(x[g0 + G], x[g1 + G]);
+    const float2 d = make_float2(dh[j], dh[j + 1]);
+    const float2 s = sigmoid_from_neg_log2_f2(__fmul2_rn(gt, splat2(-LOG2E)));
+    // silu'(g) = s (1 + g (1 - s)); silu(g) = g s
+    const float2 one_minus_s = __ffma2_rn(s, splat2(-1.0f), splat2(1.0f));
+    const float2 dsilu = __fmul2_rn(s, __ffma2_rn(gt, one_minus_s, splat2(1.0f)));
+    const float2 og = __fmul2_rn(__fmul2_rn(d, up), dsilu);
+    const float2 ou = __fmul2_rn(d, __fmul2_rn(gt, s));
+    out[g0] = og.x;
+    out[g1] = og.y;
+    out[g0 + G] = ou.x;
+    out[g1 + G] = ou.y;
   }
 }
 
@@ -1015,12 +1063,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto run_op = [&](auto code) {
           switch (static_cast<int>(code)) {
             case GEMM_EPI_OP_ADD_RESIDUAL:
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += x[j];
+              for_pairs(v, [&](float2 y, int i) { return __fadd2_rn(y, make_float2(x[2 * i], x[2 * i + 1])); });
               break;
             case GEMM_EPI_OP_MUL_GELU_TANH_GRAD:
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
+              for_pairs(v, [&](float2 y, int i) {
+                return __fmul2_rn(y, gelu_tanh_grad_f2(make_float2(x[2 * i], x[2 * i + 1])));
+              });
               break;
             case GEMM_EPI_OP_AMAX:
               if (row_ok) {
