@@ -657,6 +657,48 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
   return x[0];
 }
 
+// Column sums of a 32-row x 32-column chunk held thread = row: the chunk goes
+// back into its own TMEM columns (`taddr`: lane quad base, first column) and
+// returns in the MMA-fragment layout, where each thread holds 4 rows of 8
+// columns.  After 3 in-thread adds per column, a transpose-reduce over the 8
+// lanes that share lane % 4 (7 shuffles, where thread = row takes 31) leaves
+// lane l with the sum of column 8 (g / 2) + 2 (l % 4) + (g % 2), g = l / 4,
+// which is returned in `col`.
+__device__ __forceinline__ float tmem_column_sums(const float (&s)[32], uint32_t taddr, int lane, int& col) {
+  uint32_t w[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(s[j]);
+  ptx::tmem_st32_sync(taddr, w);
+  uint32_t a[16], b[16];
+  ptx::tmem_ld16x256_x4_pair_sync(taddr, taddr + (16u << 16), a, b);
+  // p[2i + e]: this thread's 4 rows of column 8i + 2 (lane % 4) + e
+  float p[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 lo = __fadd2_rn(make_float2(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1])),
+                                 make_float2(__uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3])));
+    const float2 hi = __fadd2_rn(make_float2(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1])),
+                                 make_float2(__uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3])));
+    const float2 t = __fadd2_rn(lo, hi);
+    p[2 * i] = t.x;
+    p[2 * i + 1] = t.y;
+  }
+  // transpose-reduce over lane bits 4, 3, 2 (value index bits 2, 1, 0)
+#pragma unroll
+  for (int s2 = 4, m = 16; s2 >= 1; s2 >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < s2; ++i) {
+      const float send = upper ? p[i] : p[i + s2];
+      const float keep = upper ? p[i + s2] : p[i];
+      p[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  const int g = lane >> 2;
+  col = 8 * (g >> 1) + 2 * (lane & 3) + (g & 1);
+  return p[0];
+}
+
 // ------------------------------------------------------------------ kernel
 
 // IN8 = 1: 8-bit operands (tcgen05 kind::f8f6f4); a K block is still one
@@ -1020,8 +1062,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             pair_combine(a, v, p.pair_g, p.pair_silu != 0);
           }
         }
-        if (c == chunks - 1) {
-          // The accumulator buffer is free for the next tile's MMAs.
+        // The accumulator buffer is free for the next tile's MMAs once the last
+        // chunk is read -- or, when column sums pass through the chunk's TMEM
+        // columns, once the last chunk's sums are done (below).
+        // (Compiled programs only: the interpreter keeps the shuffle form, which
+        // needs no extra registers.)
+        const bool tmem_col_sums = kStatic && (flags & F_COL) && !expand;
+        auto release_accumulator = [&]() {
           ptx::tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) {
@@ -1030,7 +1077,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
               ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(BAR_TEMPTY + buf), 0));
           }
-        }
+        };
+        if (c == chunks - 1 && !tmem_col_sums) release_accumulator();
 
         // ---- auxiliary tile (residual / pre-activation), this thread's row
         float x[32];
@@ -1143,8 +1191,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               float s[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) s[j] = row_ok ? v[j] : 0.0f;
-              const float tot = warp_transpose_sum(s, lane);
-              if (slab_ok && col0 + lane < p.n_out) atomicAdd(col_b + col0 + lane, tot);
+              if (!tmem_col_sums) {
+                const float tot = warp_transpose_sum(s, lane);
+                if (slab_ok && col0 + lane < p.n_out) atomicAdd(col_b + col0 + lane, tot);
+              } else {
+                // The chunk's own accumulator columns (already read) hold it.
+                const uint32_t tcol = pair_g128 ? c * 32 : paired ? c * 64 : c * 32;
+                int cj;
+                const float tot = tmem_column_sums(s, t_row + tcol, lane, cj);
+                if (slab_ok && col0 + cj < p.n_out) atomicAdd(col_b + col0 + cj, tot);
+              }
               break;
             }
             default:
@@ -1158,6 +1214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           for (int i = op_begin; i < p.n_ops; ++i) run_op(p.ops[i].code);
         }
+        if (c == chunks - 1 && tmem_col_sums) release_accumulator();
 
         // ---- TMA stores of this chunk's staged outputs
         if (flags & (F_STORE | F_E8)) {
