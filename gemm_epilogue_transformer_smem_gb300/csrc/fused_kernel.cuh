@@ -1065,9 +1065,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // The accumulator buffer is free for the next tile's MMAs once the last
         // chunk is read -- or, when column sums pass through the chunk's TMEM
         // columns, once the last chunk's sums are done (below).
-        // (Compiled programs only: the interpreter keeps the shuffle form, which
-        // needs no extra registers.)
-        const bool tmem_col_sums = kStatic && (flags & F_COL) && !expand;
+        // (Compiled programs without a pair or expanding op, whose output
+        // chunk c sits in accumulator columns 32c..32c+31; the interpreter
+        // keeps the shuffle form, which needs no extra registers.)
+        const bool tmem_col_sums = kStatic && (flags & F_COL) && !expand && !paired;
         auto release_accumulator = [&]() {
           ptx::tc_fence_before_sync();
           __syncwarp();
@@ -1196,9 +1197,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (slab_ok && col0 + lane < p.n_out) atomicAdd(col_b + col0 + lane, tot);
               } else {
                 // The chunk's own accumulator columns (already read) hold it.
-                const uint32_t tcol = pair_g128 ? c * 32 : paired ? c * 64 : c * 32;
                 int cj;
-                const float tot = tmem_column_sums(s, t_row + tcol, lane, cj);
+                const float tot = tmem_column_sums(s, t_row + c * 32, lane, cj);
                 if (slab_ok && col0 + cj < p.n_out) atomicAdd(col_b + col0 + cj, tot);
               }
               break;

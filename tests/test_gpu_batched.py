@@ -24,6 +24,8 @@ PROGRAMS = {
     "fp8": (("alpha", "bias", "relu", "amax", "store_bf16", "store_e4m3"), "kn"),
     "residual_rms": (("residual", "store_bf16", "row_rms:1e-6"), "nk"),
     "grad_colsum": (("row_scale", "gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
+    # the backward workload's compiled program: column sums through TMEM
+    "grad_colsum_static": (("gelu_tanh_grad", "store_bf16", "col_sum"), "nk"),
     "dswiglu": (("alpha", "dswiglu", "store_bf16", "amax"), "nk"),
     "rms_bwd": (("store_bf16", "col_scale", "row_dot"), "kn"),
 }
