@@ -282,6 +282,23 @@ def test_empty_problem_clears_reductions():
     assert out.amax.item() == 0.0 and torch.all(out.col_out == 0)
 
 
+def test_zero_columns_launch_nothing_and_clear_amax():
+    """N == 0: no output column, no launch; AMAX is still overwritten (0)."""
+    M, K = 64, 64
+    plan = api.Plan(M, 0, K, ["amax", "store_bf16", "col_sum"], ldb=8, ldc=8)
+    amax = torch.full((1,), 7.0, device=DEV)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
+    A = torch.zeros((M, K), device=DEV, dtype=torch.bfloat16)
+    B = torch.zeros((K, 8), device=DEV, dtype=torch.bfloat16)
+    C = torch.full((M, 8), 3.0, device=DEV, dtype=torch.bfloat16)
+    col = torch.full((8,), 5.0, device=DEV)
+    plan.run(A, B, C=C, amax=amax, col_out=col, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.query_status(ws) == 0
+    assert amax.item() == 0.0
+    assert torch.all(C == 3.0)  # nothing written outside the (empty) output
+
+
 @pytest.mark.parametrize("N", [300, 333, 7])
 def test_strided_operands_and_guard_bands(N):
     """Row strides larger than the logical width and output widths that end
