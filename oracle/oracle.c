@@ -33,7 +33,7 @@
  *    output tile, forward and backward: "CODA: ... GEMM-Epilogue"
  *    (lehuy.net), "How CODA works".
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent:
  *  - GELU is the tanh approximation 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715
  *    x^3))), evaluated as x * sigmoid(2u); its derivative is
  *    s + 2 x s (1 - s) sqrt(2/pi) (1 + 3*0.044715 x^2), s = sigmoid(2u).
