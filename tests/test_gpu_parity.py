@@ -496,6 +496,28 @@ def test_edge_chunk_stores_repeated(name, N, variant):
             check_e4m3(out.C8[:, idx].cpu().numpy(), ref8, ref["y"] * inp.fp8_scale)
 
 
+@pytest.mark.parametrize("variant", ["1sm", "2sm", "interp"])
+@pytest.mark.parametrize("name,M,N,K", [("swiglu", 520, 1040, 264), ("fp8", 520, 1040, 264),
+                                        ("backward", 520, 1040, 264), ("dswiglu", 300, 520, 200),
+                                        ("downproj", 520, 1000, 264)])
+def test_stored_outputs_are_bit_identical_across_runs(name, M, N, K, variant):
+    """The stored tensors do not depend on timing: five runs give the same
+    bits (reductions, whose atomics may add in any order, are not compared).
+    A race in the store path that moved a value by one ulp would pass the
+    tolerance checks but not this one."""
+    w = small(name, M, N, K)
+    inp = synth.make_inputs(w, DEV)
+    first = None
+    for _ in range(5):
+        plan, out = run_cuda(w, inp, debug_flags=VARIANTS[variant])
+        got = (out.C.view(torch.int16).clone(), None if out.C8 is None else out.C8.clone())
+        if first is None:
+            first = got
+        else:
+            assert torch.equal(got[0], first[0])
+            assert (got[1] is None) or torch.equal(got[1], first[1])
+
+
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("g,layout", [(2, "kn"), (4, "nk"), (8, "kn"), (16, "nk")])
 def test_dswiglu_groups_and_ops(g, layout, variant):
