@@ -342,8 +342,14 @@ typedef struct gemm_epi_rmsnorm_bwd_args {
  * capture-safe; checks sizes, pointers and alignment first. */
 GEMM_EPI_API gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bwd_args *args, void *stream);
 
-/* Synchronises `stream`, then reads the status word the last run on that
- * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT. */
+/* Synchronises `stream`, then reads the status words the last run on that
+ * workspace left: GEMM_EPI_OK or GEMM_EPI_ERR_TIMEOUT (the last-error string
+ * then names the wait and the block).  For diagnostics, the first four
+ * 32-bit words of the workspace hold: [0] bit 0 an in-kernel wait ran out,
+ * bit 1 the bounded wait for the operand loads still in flight after it
+ * also ran out; [1] which wait; [2] the block; [3] the pipeline stages whose
+ * loads the abort path settled (bits 0-7: a half that was never loaded,
+ * bits 8-15: a phase the even CTA of a pair had not armed). */
 GEMM_EPI_API gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
 
 /* Static description of a status code. */
