@@ -282,6 +282,45 @@ def test_empty_problem_clears_reductions():
     assert out.amax.item() == 0.0 and torch.all(out.col_out == 0)
 
 
+@pytest.mark.parametrize("variant", ["2sm", "interp"])
+def test_fp8_codes_saturate_like_the_oracle(variant):
+    """Outputs far beyond the e4m3 range: every code saturates to +-448
+    (0x7E / 0xFE) exactly where the oracle's does, never to NaN."""
+    M, N, K = 200, 272, 64  # e4m3 rows must start on 16-byte boundaries
+    w = synth.Workload("sat", 13, M, N, K, "kn", ("alpha", "bias", "gelu_tanh", "amax", "store_bf16", "store_e4m3"),
+                       a_std=1.0, b_std=1.0, bias_std=1.0, alpha=1.0, fp8_scale=1e4)
+    inp = synth.make_inputs(w, DEV, seed=5)
+    plan, out = run_cuda(w, inp, debug_flags=VARIANTS[variant])
+    ref = compare_rows(w, inp, out)
+    codes = out.C8.cpu().numpy()
+    assert np.all(codes[ref["c_e4m3"] == 0x7E] == 0x7E) and np.all(codes[ref["c_e4m3"] == 0xFE] == 0xFE)
+    assert (ref["c_e4m3"] == 0x7E).sum() > M * N // 4  # most codes saturated
+    assert not np.any((codes & 0x7F) == 0x7F)  # no NaN codes
+
+
+@pytest.mark.parametrize("variant", ["2sm", "interp"])
+def test_nan_input_row_propagates_and_wins_amax(variant):
+    """A NaN in one row of A makes that row's outputs NaN (bf16 NaN, e4m3 NaN
+    code) and AMAX NaN: the integer maximum over float bits orders NaN above
+    every finite value and infinity.  Every other row still matches the
+    oracle."""
+    M, N, K = 200, 272, 64
+    prog = ["gelu_tanh", "amax", "store_bf16", "store_e4m3"]
+    w = synth.Workload("nanrow", 14, M, N, K, "kn", tuple(prog), a_std=0.5, b_std=0.5, fp8_scale=8.0)
+    inp = synth.make_inputs(w, DEV, seed=6)
+    bad = 37
+    inp.A[bad, 3] = float("nan")
+    plan, out = run_cuda(w, inp, debug_flags=VARIANTS[variant])
+    c = out.C.float()
+    assert torch.isnan(c[bad]).all()
+    assert np.all((out.C8[bad].cpu().numpy() & 0x7F) == 0x7F)
+    assert np.isnan(out.amax.item())
+    keep = [r for r in range(M) if r != bad]
+    ref = oracle_problem(w, inp).rows(keep)
+    check_bf16(bits(out.C[keep]), ref["y"])
+    check_e4m3(out.C8[keep].cpu().numpy(), ref["c_e4m3"], ref["y"] * w.fp8_scale)
+
+
 def test_zero_columns_launch_nothing_and_clear_amax():
     """N == 0: no output column, no launch; AMAX is still overwritten (0)."""
     M, K = 64, 64
