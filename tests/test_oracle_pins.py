@@ -409,6 +409,21 @@ def test_amax_and_stores_consistent():
     assert oracle.to_bf16_bits([out["amax"]])[0] == out["c_bf16"].max()
 
 
+def test_nan_input_row_is_nan_and_wins_amax():
+    """A NaN operand element makes its row's outputs NaN (bf16 NaN, e4m3 NaN
+    code) and the AMAX NaN; the other rows are untouched."""
+    A = rand_bf16((6, 8))
+    B = rand_bf16((8, 16))
+    A[2, 5] = 0x7FC0  # bf16 quiet NaN
+    out = Problem(A, B, ["gelu_tanh", "amax", "store_bf16", "store_e4m3"], fp8_scale=8.0).rows()
+    assert np.all(np.isnan(out["y"][2]))
+    assert np.all((out["c_bf16"][2] & 0x7FFF) > 0x7F80)  # NaN bit patterns
+    assert np.all((out["c_e4m3"][2] & 0x7F) == 0x7F)
+    assert math.isnan(out["amax"])
+    clean = Problem(np.delete(A, 2, 0), B, ["gelu_tanh", "amax", "store_bf16"]).rows()
+    np.testing.assert_array_equal(np.delete(out["y"], 2, 0), clean["y"])
+
+
 def test_cols_match_rows():
     A = rand_bf16((9, 16))
     W = rand_bf16((12, 16))
