@@ -60,6 +60,38 @@ def test_gemm_epilogue_past_32_bit_offsets():
     del A, B, res, C
 
 
+def test_backward_epilogue_past_32_bit_offsets():
+    """gelu' of the pre-activation + bf16 store + column sums (the backward
+    program's compiled kernel, column sums through TMEM), K = 64, W stored
+    N x K: pre-activation loads and stores at offsets past 2^31, and column
+    sums over all 65600 rows."""
+    K = 64
+    g = torch.Generator(device=DEV).manual_seed(66)
+    A = torch.randn(M, K, generator=g, device=DEV, dtype=torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device=DEV) / 8).to(torch.bfloat16)
+    pre = torch.randn(M, LD, generator=g, device=DEV, dtype=torch.bfloat16)
+    C = torch.full((M, LD), 3.0, device=DEV, dtype=torch.bfloat16)
+    prog = ["gelu_tanh_grad", "store_bf16", "col_sum"]
+    plan = api.Plan(M, N, K, prog, b_layout="nk", ldc=LD, ld_aux=LD)
+    col_out = torch.empty(N, device=DEV)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
+    plan.run(A, W, preact=pre, C=C, col_out=col_out, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.query_status(ws) == 0
+    assert torch.all(C[:, N:] == 3.0), "C written past N"
+    rows = _sample_rows()
+    idx = torch.as_tensor(rows, device=DEV)
+    p_rows = oracle.Problem(bits(A[idx]), bits(W), prog, b_is_nk=True, preact=bits(pre[idx, :N]))
+    check_bf16(bits(C[idx, :N]), p_rows.rows()["y"], "C")
+    # Columns are independent: the oracle takes just the sampled columns of W
+    # and of the pre-activation, over every row.
+    cols = torch.as_tensor([0, 31, 32, 16383, 32767, 32768, 32769], device=DEV)
+    p_cols = oracle.Problem(bits(A), bits(W[cols]), prog, b_is_nk=True, preact=bits(pre[:, cols]))
+    ref = p_cols.cols(list(range(len(cols))))
+    check_cols(col_out[cols].cpu().numpy(), ref["col_stat"], np.abs(ref["y"]).sum(0))
+    del A, W, pre, C
+
+
 def test_rmsnorm_backward_past_32_bit_offsets():
     g = torch.Generator(device=DEV).manual_seed(65)
     dy = torch.randn(M, LD, generator=g, device=DEV, dtype=torch.bfloat16)
