@@ -1107,17 +1107,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // ---- the op program on output columns
         const bool full_cols = col0 + 32 <= p.n_out;
+        // The chunk's bf16 bits once STORE_BF16 has packed them: a compiled
+        // program's ROW_RMS_RSQRT squares these instead of rounding again.
+        uint32_t pk[16];
+        bool packed = false;
         // One body per op; `code` is an int (interpreted program) or an
         // integral_constant (static program), for which the switch folds.
         auto run_op = [&](auto code) {
           switch (static_cast<int>(code)) {
             case GEMM_EPI_OP_ADD_RESIDUAL:
               for_pairs(v, [&](float2 y, int i) { return __fadd2_rn(y, make_float2(x[2 * i], x[2 * i + 1])); });
+              packed = false;
               break;
             case GEMM_EPI_OP_MUL_GELU_TANH_GRAD:
               for_pairs(v, [&](float2 y, int i) {
                 return __fmul2_rn(y, gelu_tanh_grad_f2(make_float2(x[2 * i], x[2 * i + 1])));
               });
+              packed = false;
               break;
             case GEMM_EPI_OP_AMAX:
               if (row_ok) {
@@ -1137,7 +1143,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 w.z = ptx::pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
                 w.w = ptx::pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
                 *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
+                if constexpr (kStatic) {
+                  pk[4 * q] = w.x;
+                  pk[4 * q + 1] = w.y;
+                  pk[4 * q + 2] = w.z;
+                  pk[4 * q + 3] = w.w;
+                }
               }
+              packed = kStatic;
               if (col0 + 32 > p.n_al && row_ok) {  // ragged last 16-byte group
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -1182,10 +1195,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (full_cols || col0 + j < p.n_out) row_ss = fmaf(v[j], x[j], row_ss);
               break;
             case GEMM_EPI_OP_ROW_RMS_RSQRT:
+              if (packed && full_cols && !p.rms_unrounded) {
+                float2 ss = make_float2(0.0f, 0.0f);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float u = p.rms_unrounded ? v[j] : bf16_round_f(v[j]);
-                if (full_cols || col0 + j < p.n_out) row_ss = fmaf(u, u, row_ss);
+                for (int h = 0; h < 16; ++h) {
+                  const float2 u = make_float2(__uint_as_float(pk[h] << 16), __uint_as_float(pk[h] & 0xFFFF0000u));
+                  ss = __ffma2_rn(u, u, ss);
+                }
+                row_ss += ss.x + ss.y;
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const float u = p.rms_unrounded ? v[j] : bf16_round_f(v[j]);
+                  if (full_cols || col0 + j < p.n_out) row_ss = fmaf(u, u, row_ss);
+                }
               }
               break;
             case GEMM_EPI_OP_COL_SUM: {
@@ -1205,6 +1228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             default:
               apply_pointwise<32>(code, v, p, col0, p.n_out, rs_m);
+              packed = false;  // the values changed after any earlier store
               break;
           }
         };
