@@ -664,10 +664,18 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32], int lane) {
 // lanes that share lane % 4 (7 shuffles, where thread = row takes 31) leaves
 // lane l with the sum of column 8 (g / 2) + 2 (l % 4) + (g % 2), g = l / 4,
 // which is returned in `col`.
-__device__ __forceinline__ float tmem_column_sums(const float (&s)[32], uint32_t taddr, int lane, int& col) {
+// Rows with row_ok false (past M) count as zero; `all_rows` (warp-uniform)
+// says that the warp has none, so the chunk goes to TMEM unmasked.
+__device__ __forceinline__ float tmem_column_sums(const float (&s)[32], bool row_ok, bool all_rows, uint32_t taddr,
+                                                  int lane, int& col) {
   uint32_t w[32];
+  if (all_rows) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(s[j]);
+    for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(s[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) w[j] = row_ok ? __float_as_uint(s[j]) : 0u;
+  }
   ptx::tmem_st32_sync(taddr, w);
   uint32_t a[16], b[16];
   ptx::tmem_ld16x256_x4_pair_sync(taddr, taddr + (16u << 16), a, b);
@@ -1212,16 +1220,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               break;
             case GEMM_EPI_OP_COL_SUM: {
-              float s[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) s[j] = row_ok ? v[j] : 0.0f;
               if (!tmem_col_sums) {
+                float s[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[j] = row_ok ? v[j] : 0.0f;
                 const float tot = warp_transpose_sum(s, lane);
                 if (slab_ok && col0 + lane < p.n_out) atomicAdd(col_b + col0 + lane, tot);
               } else {
                 // The chunk's own accumulator columns (already read) hold it.
                 int cj;
-                const float tot = tmem_column_sums(s, t_row + c * 32, lane, cj);
+                const float tot = tmem_column_sums(v, row_ok, slab_row0 + 32 <= p.M, t_row + c * 32, lane, cj);
                 if (slab_ok && col0 + cj < p.n_out) atomicAdd(col_b + col0 + cj, tot);
               }
               break;
