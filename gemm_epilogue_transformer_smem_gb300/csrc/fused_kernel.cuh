@@ -492,6 +492,10 @@ __device__ __forceinline__ float bf16_round_f(float x) {
   return __uint_as_float(h << 16);
 }
 
+// Internal op of compiled programs: SCALE_ALPHA directly followed by
+// ADD_BIAS_COL, as one fused multiply-add (not a public op code).
+constexpr int OP_ALPHA_THEN_BIAS = 0x70;
+
 // Element-wise ops that may run on accumulator columns (before the pair op)
 // or on output columns.  Columns of v[j]: col0 + j; `ncols` bounds the bias.
 // `code` is an int, or a std::integral_constant whose switch folds away.
@@ -504,6 +508,22 @@ __device__ __forceinline__ void apply_pointwise(CodeT code, float (&v)[NV], cons
       for_pairs(v, [&](float2 y, int) { return __fmul2_rn(y, a); });
       break;
     }
+    case OP_ALPHA_THEN_BIAS:
+      if (col0 + NV <= ncols) {
+        const float2 a = splat2(p.alpha);
+        const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);
+        for_pairs(v, [&](float2 y, int i) {
+          const float4 b = __ldg(b4 + i / 2);
+          return __ffma2_rn(y, a, (i & 1) ? make_float2(b.z, b.w) : make_float2(b.x, b.y));
+        });
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          v[j] *= p.alpha;
+          if (col0 + j < ncols) v[j] += __ldg(p.bias + col0 + j);
+        }
+      }
+      break;
     case GEMM_EPI_OP_ADD_BIAS_COL:
       if (col0 + NV <= ncols) {
         const float4* b4 = reinterpret_cast<const float4*>(p.bias + col0);
@@ -954,7 +974,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* e80_ptr = smem + L::OFF_E8 + ew * E8_BUFS * E8_BUF_BYTES;
     const int op_begin = paired ? pair_at + 1 : expand ? expand_at + 1 : 0;
 
-    uint32_t amax_bits = 0;
+    float amax_f = 0.0f;  // max |y| so far; a NaN sticks (NaN wins, as in the integer maximum below)
     uint32_t gchunk = 0;                 // this warp's running chunk number
     bool ok = true;
     int local = 0;
@@ -1138,7 +1158,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                   if (full_cols || col0 + j < p.n_out)
-                    amax_bits = max(amax_bits, __float_as_uint(fabsf(v[j])));
+                    amax_f = ptx::max_abs_nan(amax_f, v[j]);
               }
               break;
             case GEMM_EPI_OP_STORE_BF16: {
@@ -1241,8 +1261,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         };
         if constexpr (kStatic) {
-          static_for<prog_post_begin<Prog>(), prog_n<Prog>()>(
-              [&](auto I) { run_op(std::integral_constant<int, Prog::code_of(decltype(I)::value)>{}); });
+          static_for<prog_post_begin<Prog>(), prog_n<Prog>()>([&](auto I) {
+            constexpr int i = decltype(I)::value;
+            constexpr int code = Prog::code_of(i);
+            constexpr bool bias_next = i + 1 < prog_n<Prog>() && Prog::code_of(i + 1) == GEMM_EPI_OP_ADD_BIAS_COL;
+            constexpr bool alpha_before = i > prog_post_begin<Prog>() && Prog::code_of(i - 1) == GEMM_EPI_OP_SCALE_ALPHA;
+            if constexpr (code == GEMM_EPI_OP_SCALE_ALPHA && bias_next)
+              run_op(std::integral_constant<int, OP_ALPHA_THEN_BIAS>{});
+            else if constexpr (!(code == GEMM_EPI_OP_ADD_BIAS_COL && alpha_before))  // else folded in above
+              run_op(std::integral_constant<int, code>{});
+          });
         } else {
           for (int i = op_begin; i < p.n_ops; ++i) run_op(p.ops[i].code);
         }
@@ -1304,6 +1332,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) ptx::bulk_wait_group<0>();
     if (flags & F_AMAX) {
 #pragma unroll
+      // Non-negative floats order like their bit patterns, and NaN's bits
+      // exceed infinity's: one integer maximum across the warp and the grid.
+      uint32_t amax_bits = __float_as_uint(amax_f);
       for (int s = 16; s >= 1; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, s));
       if (lane == 0 && amax_bits != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.amax), amax_bits);
     }

@@ -395,6 +395,14 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// max(m, |x|) where a NaN in either input gives NaN (the NaN-propagating
+// form of max; |x| may fold into the instruction's operand).
+__device__ __forceinline__ float max_abs_nan(float m, float x) {
+  float r;
+  asm("{\n\t.reg .f32 t;\n\tabs.f32 t, %2;\n\tmax.NaN.f32 %0, %1, t;\n\t}" : "=f"(r) : "f"(m), "f"(x));
+  return r;
+}
+
 // 2^x on the special-function unit.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
