@@ -11,16 +11,18 @@
 //
 // How, on sm_103a:
 //   warp 0      TMA producer: A (K-major, 128x64 box) and B (K-major 256x64
-//               box, or four MN-major 64x64 boxes) into a STAGES-deep ring of
-//               128B-swizzled shared-memory stages, mbarrier transaction counts.
+//               box, or four MN-major 64x64 boxes) into a ring of 128B-swizzled
+//               shared-memory slots, one K-block each; a stage of two slots
+//               shares one full barrier (mbarrier transaction counts), each
+//               slot has its own empty barrier.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators),
 //               then one lane issues tcgen05.mma (N=256, K=16) and commits
-//               each stage back to the producer and each finished
+//               each slot back to the producer and each finished
 //               accumulator to the epilogue.
 // Two main-loop shapes share the code (template parameter CG):
-//   CG = 1  one CTA per 128 x 256 tile, M = 128 MMAs, 4 stages of 48 KB.
+//   CG = 1  one CTA per 128 x 256 tile, M = 128 MMAs, 4 slots of 48 KB.
 //   CG = 2  a cluster of two CTAs per 256 x 256 tile: each CTA stages its
-//           128 rows of A and its 128 columns of B (6 stages of 32 KB), the
+//           128 rows of A and its 128 columns of B (6 slots of 32 KB), the
 //           even CTA issues tcgen05.mma.cta_group::2 (M = 256) for the pair
 //           and multicasts its commits to both CTAs; each CTA's epilogue
 //           drains the 128 x 256 accumulator in its own TMEM.  Each SM then
@@ -62,7 +64,7 @@ constexpr int EPI_BUFS = 3;   // bf16 output staging buffers per epilogue warp
 constexpr int E8_BUFS = 2;    // e4m3 staging buffers per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;
 
-constexpr uint32_t A_STAGE_BYTES = BLOCK_M * BLOCK_K * 2;
+constexpr uint32_t A_KB_BYTES = BLOCK_M * BLOCK_K * 2;  // one K-block of A
 constexpr uint32_t B_MN_BOX_BYTES = 64 * BLOCK_K * 2;  // one 64-column MN-major box
 constexpr uint32_t EPI_BUF_BYTES = 32 * CHUNK * 2;     // 32 rows x 64 bytes
 constexpr uint32_t E8_BUF_BYTES = 32 * CHUNK;          // 32 rows x 32 bytes
@@ -71,9 +73,19 @@ constexpr uint64_t DRAIN_LIMIT_NS = 20000000ull;       // bound of the abort-pat
 // Shared-memory map of one CTA when CG CTAs share a tile.
 template <int CG>
 struct Smem {
-  static constexpr int STAGES = CG == 1 ? 4 : 6;
+  // The operand ring holds SLOTS K-blocks.  A stage is KB_PER_STAGE
+  // consecutive slots under one full barrier: the CTA pair's MMA warp waits
+  // once per eight MMAs.  Each slot has its own empty barrier and is
+  // refilled as soon as its four MMAs are done, which keeps the loads as far
+  // ahead as with one K-block per stage.  The single-CTA loop runs the
+  // memory-bound small-M problems and waits per K-block.
+  static constexpr int SLOTS = CG == 1 ? 4 : 6;
+  static constexpr int KB_PER_STAGE = CG == 2 ? 2 : 1;
+  static constexpr int STAGES = SLOTS / KB_PER_STAGE;
   static constexpr int B_COLS = BLOCK_N / CG;  // B columns (N) this CTA stages
-  static constexpr uint32_t B_STAGE_BYTES = B_COLS * BLOCK_K * 2;
+  static constexpr uint32_t B_KB_BYTES = B_COLS * BLOCK_K * 2;  // one K-block of B
+  static constexpr uint32_t A_STAGE_BYTES = KB_PER_STAGE * A_KB_BYTES;
+  static constexpr uint32_t B_STAGE_BYTES = KB_PER_STAGE * B_KB_BYTES;
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
@@ -81,7 +93,7 @@ struct Smem {
   static constexpr uint32_t OFF_BAR = OFF_E8 + NUM_EPI_WARPS * E8_BUFS * E8_BUF_BYTES;
   static constexpr uint32_t BAR_FULL = 0;
   static constexpr uint32_t BAR_EMPTY = BAR_FULL + STAGES;
-  static constexpr uint32_t BAR_TFULL = BAR_EMPTY + STAGES;
+  static constexpr uint32_t BAR_TFULL = BAR_EMPTY + SLOTS;
   static constexpr uint32_t BAR_TEMPTY = BAR_TFULL + 2;
   static constexpr uint32_t BAR_DRAIN = BAR_TEMPTY + 2;
   static constexpr uint32_t NUM_BARS = BAR_DRAIN + 1;
@@ -346,9 +358,17 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Operand loads issued into one stage: a 2-bit count per stage (mod 4).
-__device__ __forceinline__ uint32_t count_load(uint32_t cnt, uint32_t stage) {
-  const uint32_t sh = 2u * stage;
+// Test hooks (first CTA, first tile): loads the producer leaves out so that
+// a bounded wait runs out.  A skipped load is neither counted nor, for the
+// first K-block of a stage, armed.
+__device__ __forceinline__ bool skip_load_hook(uint32_t flags, int ks, int kb) {
+  return ((flags & GEMM_EPI_DEBUG_SKIP_FIRST_LOAD) && ks == 0) ||
+         ((flags & GEMM_EPI_DEBUG_SKIP_SECOND_LOAD) && kb == 1);
+}
+
+// Operand loads issued into one ring slot: a 2-bit count per slot (mod 4).
+__device__ __forceinline__ uint32_t count_load(uint32_t cnt, uint32_t slot) {
+  const uint32_t sh = 2u * slot;
   return (cnt & ~(3u << sh)) | ((((cnt >> sh) & 3u) + 1u) & 3u) << sh;
 }
 
@@ -356,46 +376,62 @@ __device__ __forceinline__ uint32_t count_load(uint32_t cnt, uint32_t stage) {
 // CTA group's shared memory has landed, so that no copy writes into shared
 // memory after the group exits.  Runs in the CTA that owns the full
 // barriers (the even CTA of a pair), once every role of both CTAs is done.
-// `own` and `peer` hold the per-stage load counts of this CTA and of the odd
-// CTA, whose loads complete on this CTA's barriers.  The producers advance
-// in step (each waits on an empty barrier that the pair's MMA commit frees),
-// so per stage the counts differ by at most one:
-//   equal         the last phase holds both halves: wait for it;
-//   own = peer+1  this CTA armed a phase the odd CTA never loaded into:
-//                 count the missing half as arrived, then wait;
-//   peer = own+1  the odd CTA loaded into a phase this CTA never armed
-//                 (armed here now for both halves, this CTA's half counted
-//                 as arrived), then wait for the odd CTA's bytes.
+// `own` and `peer` hold the per-slot load counts of this CTA and of the odd
+// CTA, whose loads complete on this CTA's barriers.  This CTA arms a stage's
+// full barrier, for every slot of the stage in both CTAs, when it loads the
+// stage's first slot, so that slot's count a0 is the number of phases armed.
+// A slot is reloaded only after the pair's MMAs used it, which needed both
+// CTAs' previous loads, and each CTA fills a stage's slots in order; so every
+// count of the stage is a0 - 1, a0 or (odd CTA only) a0 + 1:
+//   none at a0 + 1  phase a0 is the last one armed: the slots never loaded
+//                   for it are counted as arrived, then it is waited for;
+//   some at a0 + 1  the odd CTA loaded into a phase this CTA never armed:
+//                   it is armed now, every slot not loaded for it counted
+//                   as arrived, and waited for.
 // Records status bit 1 when a wait ran out and, in status word 3, the stages
 // settled each way (bits 0-7 and 8-15).
-template <int CG, int STAGES>
+template <int CG, int STAGES, int KPS>
 __device__ __noinline__ void drain_operand_loads(uint32_t bar_full0, uint32_t own, uint32_t peer,
-                                                 uint32_t half_bytes, uint32_t* status) {
+                                                 uint32_t slot_bytes, uint32_t* status) {
   bool late = false;
   uint32_t settled = 0;
+  constexpr uint32_t SLOTS_PER_PHASE = CG * KPS;  // slot loads one phase expects
 #pragma unroll 1
   for (uint32_t s = 0; s < STAGES; ++s) {
     const uint32_t bar = bar_full0 + 8u * s;
-    uint32_t n = (own >> (2u * s)) & 3u;
-    if (CG == 2) {
-      const uint32_t np = (peer >> (2u * s)) & 3u;
-      const uint32_t d = (n - np) & 3u;
-      if (d == 1u) {
-        ptx::mbar_complete_tx(bar, half_bytes);
-        settled |= 1u << s;
-      } else if (d == 3u) {
-        ptx::mbar_arrive_expect_tx(bar, 2u * half_bytes);
-        ptx::mbar_complete_tx(bar, half_bytes);
-        settled |= 1u << (8u + s);
-        n = np;
-      } else if (d == 2u) {
-        late = true;  // not reachable when the producers keep in step
-        continue;
+    const uint32_t a0 = (own >> (2u * s * KPS)) & 3u;
+    uint32_t at_a0 = 0, ahead = 0;
+    bool odd = false;
+    for (uint32_t h = 0; h < KPS; ++h) {
+      const uint32_t sh = 2u * (s * KPS + h);
+      if (((own >> sh) & 3u) == a0) ++at_a0;
+      if (CG == 2) {
+        const uint32_t d = (((peer >> sh) & 3u) - a0) & 3u;
+        if (d == 0u)
+          ++at_a0;
+        else if (d == 1u)
+          ++ahead;
+        else if (d == 2u)
+          odd = true;  // not reachable when the producers keep in step
       }
     }
-    // The last phase this stage was loaded in has parity (n - 1) & 1; with no
-    // load at all that names the phase before the first, which tests complete.
-    if (!drain_wait(bar, (n + 1u) & 1u, DRAIN_LIMIT_NS)) late = true;
+    if (odd) {
+      late = true;
+      continue;
+    }
+    uint32_t phases = a0;  // phases armed once settled (mod 4)
+    if (ahead) {
+      ptx::mbar_arrive_expect_tx(bar, SLOTS_PER_PHASE * slot_bytes);
+      ptx::mbar_complete_tx(bar, (SLOTS_PER_PHASE - ahead) * slot_bytes);
+      settled |= 1u << (8u + s);
+      phases = a0 + 1u;
+    } else if (at_a0 < SLOTS_PER_PHASE) {
+      ptx::mbar_complete_tx(bar, (SLOTS_PER_PHASE - at_a0) * slot_bytes);
+      settled |= 1u << s;
+    }
+    // The last phase armed has parity (phases - 1) & 1; with no load at all
+    // that names the phase before the first, which tests complete.
+    if (!drain_wait(bar, (phases + 1u) & 1u, DRAIN_LIMIT_NS)) late = true;
   }
   if (late) atomicOr(status, 2u);
   if (settled) atomicOr(status + 3, settled);
@@ -742,8 +778,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                const __grid_constant__ KernelParams p) {
   using L = Smem<CG>;
   constexpr int STAGES = L::STAGES;
+  constexpr int KPS = L::KB_PER_STAGE;
   constexpr int TILE_M = BLOCK_M * CG;  // rows of one tile (the whole CTA group)
-  constexpr int K_STEP = IN8 ? 2 * BLOCK_K : BLOCK_K;  // K elements per stage
+  constexpr int K_STEP = IN8 ? 2 * BLOCK_K : BLOCK_K;  // K elements per K-block
   constexpr uint32_t BAR_FULL = L::BAR_FULL, BAR_EMPTY = L::BAR_EMPTY, BAR_TFULL = L::BAR_TFULL,
                      BAR_TEMPTY = L::BAR_TEMPTY, BAR_DRAIN = L::BAR_DRAIN;
   extern __shared__ uint8_t smem_raw[];
@@ -754,11 +791,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-  // misc[0] TMEM base, misc[1] abort flag, misc[2] the odd CTA's per-stage
+  // misc[0] TMEM base, misc[1] abort flag, misc[2] the odd CTA's per-slot
   // load counts (written there by the odd CTA of a pair).
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
-  uint32_t load_cnt = 0;  // producer lane: operand loads issued per stage (2 bits each)
+  uint32_t load_cnt = 0;  // producer lane: operand loads issued per ring slot (2 bits each)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -767,10 +804,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_groups = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(bar(BAR_FULL + s), 1);
-      ptx::mbar_init(bar(BAR_EMPTY + s), 1);
-    }
+    for (uint32_t s = 0; s < STAGES; ++s) ptx::mbar_init(bar(BAR_FULL + s), 1);
+    for (uint32_t s = 0; s < L::SLOTS; ++s) ptx::mbar_init(bar(BAR_EMPTY + s), 1);
     for (uint32_t b = 0; b < 2; ++b) {
       ptx::mbar_init(bar(BAR_TFULL + b), 1);
       ptx::mbar_init(bar(BAR_TEMPTY + b), NUM_EPI_WARPS * CG);  // every epilogue warp of the group
@@ -805,6 +840,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && p.num_k_blocks > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      const int num_steps = (p.num_k_blocks + KPS - 1) / KPS;  // stages per tile
       for (int t = group; ok && t < p.num_tiles; t += num_groups) {
         int bt, mb, nb;
         tile_coords(p, t, bt, mb, nb);
@@ -815,19 +851,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the same columns of B2 (accumulator columns 128..255).
         const int b_col = p.dual ? nb * (BLOCK_N / 2) : nb * BLOCK_N + rank * L::B_COLS;
         const CUtensorMap* tmb_own = (p.dual && rank == 1) ? &tm_b2 : &tm_b;  // 2-SM: one operand per CTA
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!wait_bar<CG>(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
-            ok = false;
-            break;
-          }
-          const bool skip = (p.debug_flags & GEMM_EPI_DEBUG_SKIP_FIRST_LOAD) && blockIdx.x == 0 &&
-                            t == group && kb == 0;
-          if (!skip) {
-            const uint32_t fb = bar(BAR_FULL + stage);
-            const uint32_t sa = sbase + L::OFF_A + stage * A_STAGE_BYTES;
-            const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
+        const bool hooks = (p.debug_flags & (GEMM_EPI_DEBUG_SKIP_FIRST_LOAD | GEMM_EPI_DEBUG_SKIP_SECOND_LOAD)) &&
+                           blockIdx.x == 0 && t == group;
+        for (int ks = 0; ok && ks < num_steps; ++ks) {
+          const uint32_t fb = bar(BAR_FULL + stage);
+#pragma unroll
+          for (int h = 0; h < KPS; ++h) {
+            const uint32_t slot = stage * KPS + h;
+            if (!wait_bar<CG>(bar(BAR_EMPTY + slot), phase ^ 1u, abort_flag, p, W_PRODUCER_EMPTY)) {
+              ok = false;
+              break;
+            }
+            if (hooks && skip_load_hook(p.debug_flags, ks, ks * KPS + h)) continue;
+            if (h == 0) {
+              // The stage's full barrier expects all of its slots; with a
+              // CTA pair both CTAs' halves complete on the even CTA's.
+              if (CG == 1)
+                ptx::mbar_arrive_expect_tx(fb, L::A_STAGE_BYTES + L::B_STAGE_BYTES);
+              else if (rank == 0)
+                ptx::mbar_arrive_expect_tx(fb, 2u * (L::A_STAGE_BYTES + L::B_STAGE_BYTES));
+            }
+            // A slot past the last K-block (odd count) loads the last one
+            // again, so that every stage carries the same bytes; its MMAs
+            // are not issued.
+            const int kb = min(ks * KPS + h, p.num_k_blocks - 1);
+            const uint32_t sa = sbase + L::OFF_A + stage * L::A_STAGE_BYTES + h * A_KB_BYTES;
+            const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES + h * L::B_KB_BYTES;
             if (CG == 1) {
-              ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + L::B_STAGE_BYTES);
               ptx::tma_load_3d(sa, &tm_a, fb, kb * K_STEP, a_row, za);
               if (p.b_kn) {
 #pragma unroll
@@ -845,10 +895,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tma_load_3d(sb, &tm_b, fb, kb * K_STEP, b_col, zb);
               }
             } else {
-              // Both CTAs' halves complete on the even CTA's full barrier,
-              // which expects the bytes of the whole pair.
               const uint32_t fb0 = ptx::mapa_shared(fb, 0);
-              if (rank == 0) ptx::mbar_arrive_expect_tx(fb, 2u * (A_STAGE_BYTES + L::B_STAGE_BYTES));
               ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * K_STEP, a_row, za);
               if (p.b_kn) {
 #pragma unroll
@@ -858,7 +905,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tma_load_3d_cg2(sb, tmb_own, fb0, kb * K_STEP, b_col, zb);
               }
             }
-            load_cnt = count_load(load_cnt, stage);
+            load_cnt = count_load(load_cnt, slot);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -877,6 +924,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && rank == 0) {  // the even CTA issues for the whole group
       uint32_t stage = 0, phase = 0;
       bool ok = true, any_mma = false;
+      const int num_steps = (p.num_k_blocks + KPS - 1) / KPS;
       int local = 0;
       for (int t = group; ok && t < p.num_tiles; t += num_groups, ++local) {
         const uint32_t buf = local & 1, use = local >> 1;
@@ -895,39 +943,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           continue;
         }
         const uint32_t d_tmem = tmem_base + buf * BLOCK_N;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int ks = 0; ks < num_steps; ++ks) {
           if (!wait_bar<CG>(bar(BAR_FULL + stage), phase, abort_flag, p, W_MMA_FULL)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after_sync();
-          const uint32_t sa = sbase + L::OFF_A + stage * A_STAGE_BYTES;
-          const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES;
-          // Each MMA consumes 32 bytes of every operand row: 16 bf16 or 32
-          // FP8 elements, so both kinds step through a stage the same way.
 #pragma unroll
-          for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
-            const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
-            const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
-                                       : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
-            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-            if constexpr (CG == 1) {
-              if constexpr (IN8)
-                ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, acc);
-              else
-                ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, acc);
-            } else {
-              if constexpr (IN8)
-                ptx::mma_f8_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
-              else
-                ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
+          for (int h = 0; h < KPS; ++h) {
+            if (ks * KPS + h < p.num_k_blocks) {
+              const uint32_t sa = sbase + L::OFF_A + stage * L::A_STAGE_BYTES + h * A_KB_BYTES;
+              const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES + h * L::B_KB_BYTES;
+              // Each MMA consumes 32 bytes of every operand row: 16 bf16 or 32
+              // FP8 elements, so both kinds step through a K-block the same way.
+#pragma unroll
+              for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
+                const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
+                const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
+                                           : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
+                const uint32_t acc = (ks | h | k) != 0 ? 1u : 0u;
+                if constexpr (CG == 1) {
+                  if constexpr (IN8)
+                    ptx::mma_f8_ss(d_tmem, ad, bd, p.idesc, acc);
+                  else
+                    ptx::mma_f16_ss(d_tmem, ad, bd, p.idesc, acc);
+                } else {
+                  if constexpr (IN8)
+                    ptx::mma_f8_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
+                  else
+                    ptx::mma_f16_ss_cg2(d_tmem, ad, bd, p.idesc, acc);
+                }
+              }
             }
+            // the slot is free once its MMAs are done
+            if (CG == 1)
+              ptx::mma_commit(bar(BAR_EMPTY + stage * KPS + h));
+            else
+              ptx::mma_commit_cg2_multicast(bar(BAR_EMPTY + stage * KPS + h), 0x3);
           }
           any_mma = true;
-          if (CG == 1)
-            ptx::mma_commit(bar(BAR_EMPTY + stage));
-          else
-            ptx::mma_commit_cg2_multicast(bar(BAR_EMPTY + stage), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -1331,10 +1385,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---- teardown of the epilogue warp
     if (lane == 0) ptx::bulk_wait_group<0>();
     if (flags & F_AMAX) {
-#pragma unroll
       // Non-negative floats order like their bit patterns, and NaN's bits
       // exceed infinity's: one integer maximum across the warp and the grid.
       uint32_t amax_bits = __float_as_uint(amax_f);
+#pragma unroll
       for (int s = 16; s >= 1; s >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, s));
       if (lane == 0 && amax_bits != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.amax), amax_bits);
     }
@@ -1349,8 +1403,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   else
     __syncthreads();
   if (threadIdx.x == 0 && rank == 0 && *abort_flag && p.num_k_blocks > 0)
-    drain_operand_loads<CG, STAGES>(bar(BAR_FULL), load_cnt, CG == 2 ? misc[2] : 0u,
-                                    A_STAGE_BYTES + L::B_STAGE_BYTES, p.status);
+    drain_operand_loads<CG, STAGES, KPS>(bar(BAR_FULL), load_cnt, CG == 2 ? misc[2] : 0u,
+                                         A_KB_BYTES + L::B_KB_BYTES, p.status);
   __syncwarp();
   if (CG == 2)
     ptx::cluster_sync();  // no CTA of the pair releases TMEM or smem the other still uses

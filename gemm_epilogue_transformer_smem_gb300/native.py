@@ -61,6 +61,7 @@ GEMM_EPI_DEBUG_SKIP_FIRST_LOAD = 1
 GEMM_EPI_DEBUG_FORCE_1SM = 2
 GEMM_EPI_DEBUG_FORCE_2SM = 4
 GEMM_EPI_DEBUG_FORCE_INTERPRETER = 8
+GEMM_EPI_DEBUG_SKIP_SECOND_LOAD = 16
 GEMM_EPI_NO_ALLOC_SCRATCH_BYTES = 65536
 
 

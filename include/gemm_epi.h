@@ -245,9 +245,17 @@ typedef struct gemm_epi_args {
     const float *col_scale;   /* MUL_COL_SCALE: fp32, one value per column at its point of use */
 } gemm_epi_args;
 
-/* Test hook: the producer skips the first operand load of the first CTA so
- * that the consumer's bounded wait runs out (nothing is left in flight). */
+/* Test hook: the first CTA's producer skips the operand loads of the first
+ * pipeline stage of its first tile (two K-blocks on the CTA-pair loop, one
+ * on the single-CTA loop) and never arms that stage's full barrier, so that
+ * the MMA warp's bounded wait runs out. */
 #define GEMM_EPI_DEBUG_SKIP_FIRST_LOAD 1u
+/* Test hook: as above, but only the first tile's second K-block is not
+ * loaded.  On the CTA-pair loop it shares a stage with the first, whose
+ * barrier is then armed and stays short of those bytes: the abort path
+ * settles a partly loaded stage.  On the single-CTA loop it is a stage of
+ * its own, never armed. */
+#define GEMM_EPI_DEBUG_SKIP_SECOND_LOAD 16u
 /* Test hooks: run the 1-SM main loop (one CTA per 128 x 256 tile) or the
  * 2-SM one (a CTA pair per 256 x 256 tile) whatever M is.  By default the
  * 2-SM loop runs when M > 128. */
@@ -348,8 +356,8 @@ GEMM_EPI_API gemm_epi_status gemm_epi_rmsnorm_backward(const gemm_epi_rmsnorm_bw
  * 32-bit words of the workspace hold: [0] bit 0 an in-kernel wait ran out,
  * bit 1 the bounded wait for the operand loads still in flight after it
  * also ran out; [1] which wait; [2] the block; [3] the pipeline stages whose
- * loads the abort path settled (bits 0-7: a half that was never loaded,
- * bits 8-15: a phase the even CTA of a pair had not armed). */
+ * loads the abort path settled (bits 0-7: a stage with K-blocks that were
+ * never loaded, bits 8-15: a phase the even CTA of a pair had not armed). */
 GEMM_EPI_API gemm_epi_status gemm_epi_query_status(gemm_epi_handle h, const void *workspace, void *stream);
 
 /* Static description of a status code. */

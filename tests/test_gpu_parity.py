@@ -261,7 +261,7 @@ def test_row_scale_rewrite_identity():
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 256, 8), (127, 264, 64), (129, 8, 72), (64, 64, 0),
-                                   (300, 520, 0)])
+                                   (300, 520, 0), (260, 296, 40), (129, 264, 520)])
 def test_edge_shapes(M, N, K, variant):
     w = synth.Workload("edge", 12, M, N, K, "kn", ("alpha", "bias", "gelu_tanh", "amax", "store_bf16"),
                        a_std=0.5, b_std=0.5, bias_std=0.1, alpha=1.5)
@@ -381,25 +381,36 @@ def test_misaligned_and_missing_buffers_rejected():
     assert e.value.status == native.GEMM_EPI_ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("hook", ["stage", "second_kblock"])
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
-def test_bounded_wait_reports_timeout_and_context_survives(variant):
-    """A load the producer deliberately never issues makes the MMA warp's
+def test_bounded_wait_reports_timeout_and_context_survives(variant, hook):
+    """Loads the producer deliberately never issues make the MMA warp's
     bounded wait run out; the kernel reports it and exits cleanly."""
     w = small("tiny", 512, 512, 256)
     inp = synth.make_inputs(w, DEV)
     plan = api.Plan(w.M, w.N, w.K, w.program)
     out = api.allocate_outputs(plan, DEV)
-    api.run_program(plan, inp.A, inp.B, out, bias=inp.bias, timeout_ms=50,
-                    debug_flags=native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD | VARIANTS[variant])
+    flag = native.GEMM_EPI_DEBUG_SKIP_FIRST_LOAD if hook == "stage" else native.GEMM_EPI_DEBUG_SKIP_SECOND_LOAD
+    api.run_program(plan, inp.A, inp.B, out, bias=inp.bias, timeout_ms=50, debug_flags=flag | VARIANTS[variant])
     torch.cuda.synchronize()
     assert plan.query_status(out.workspace) == native.GEMM_EPI_ERR_TIMEOUT
     # Status words: [0] bit 0 a wait ran out, bit 1 the drain of the operand
-    # loads after it also ran out; [3] the stages the drain settled.  On the
-    # CTA-pair kernel the even CTA skipped arming stage 0, into which the odd
-    # CTA still loaded: the drain arms it and waits for those bytes (bit 8).
+    # loads after it also ran out; [1] the wait that ran out first (2: the
+    # MMA warp's for the stage, 4: the epilogue's for the accumulator, which
+    # started as early); [3] the stages the drain settled.
+    #   stage: the first CTA never armed stage 0.  On the CTA-pair kernel the
+    #     odd CTA still loaded into it: the drain arms it and waits for those
+    #     bytes (bit 8); alone, nothing was loaded and nothing is settled.
+    #   second_kblock: on the CTA pair, stage 0 (two K-blocks) is armed and
+    #     one K-block short: the drain counts the missing bytes as arrived
+    #     (bit 0); alone, that K-block is stage 1, never armed.
     words = out.workspace[:16].view(torch.int32).cpu().tolist()
     assert words[0] & 1 and not words[0] & 2, words
-    assert words[3] == (0 if "1sm" in variant else 1 << 8), words
+    assert words[1] in (2, 4), words
+    if "1sm" in variant:
+        assert words[3] == 0, words
+    else:
+        assert words[3] == (1 << 8 if hook == "stage" else 1), words
     # The context still works: a normal run afterwards is correct.
     api.run_program(plan, inp.A, inp.B, out, bias=inp.bias)
     torch.cuda.synchronize()
