@@ -944,6 +944,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const uint32_t d_tmem = tmem_base + buf * BLOCK_N;
         for (int ks = 0; ks < num_steps; ++ks) {
+          // Everything the stage's MMAs need but its data is computed before
+          // the wait: the time from a completed barrier to the first MMA is
+          // on the tensor pipe's critical path.  The descriptors of the
+          // stage's first K block step by 32 bytes per MMA (K-major) or by 16
+          // rows of 128 bytes (MN-major B); the address field counts 16 bytes.
+          const uint64_t a_d0 = smem_desc_sw128(sbase + L::OFF_A + stage * L::A_STAGE_BYTES, 16, 1024);
+          const uint64_t b_d0 =
+              smem_desc_sw128(sbase + L::OFF_B + stage * L::B_STAGE_BYTES, p.b_kn ? B_MN_BOX_BYTES : 16u, 1024);
+          const uint32_t b_k = p.b_kn ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+          const int kb_left = p.num_k_blocks - ks * KPS;  // K blocks of the tile from this stage on
+          const uint32_t empty0 = bar(BAR_EMPTY + stage * KPS);
           if (!wait_bar<CG>(bar(BAR_FULL + stage), phase, abort_flag, p, W_MMA_FULL)) {
             ok = false;
             break;
@@ -951,16 +962,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_after_sync();
 #pragma unroll
           for (int h = 0; h < KPS; ++h) {
-            if (ks * KPS + h < p.num_k_blocks) {
-              const uint32_t sa = sbase + L::OFF_A + stage * L::A_STAGE_BYTES + h * A_KB_BYTES;
-              const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES + h * L::B_KB_BYTES;
+            if (h < kb_left) {
               // Each MMA consumes 32 bytes of every operand row: 16 bf16 or 32
-              // FP8 elements, so both kinds step through a K-block the same way.
+              // FP8 elements, so both kinds step through a K block the same way.
 #pragma unroll
               for (int k = 0; k < BLOCK_K / UMMA_K; ++k) {
-                const uint64_t ad = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, 1024);
-                const uint64_t bd = p.b_kn ? smem_desc_sw128(sb + k * (UMMA_K * 128), B_MN_BOX_BYTES, 1024)
-                                           : smem_desc_sw128(sb + k * (UMMA_K * 2), 16, 1024);
+                const uint64_t ad = a_d0 + ((h * A_KB_BYTES + k * (UMMA_K * 2)) >> 4);
+                const uint64_t bd = b_d0 + ((h * L::B_KB_BYTES) >> 4) + k * b_k;
                 const uint32_t acc = (ks | h | k) != 0 ? 1u : 0u;
                 if constexpr (CG == 1) {
                   if constexpr (IN8)
@@ -977,9 +985,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             // the slot is free once its MMAs are done
             if (CG == 1)
-              ptx::mma_commit(bar(BAR_EMPTY + stage * KPS + h));
+              ptx::mma_commit(empty0 + 8u * h);
             else
-              ptx::mma_commit_cg2_multicast(bar(BAR_EMPTY + stage * KPS + h), 0x3);
+              ptx::mma_commit_cg2_multicast(empty0 + 8u * h, 0x3);
           }
           any_mma = true;
           if (++stage == STAGES) {
