@@ -12,9 +12,10 @@
 // How, on sm_103a:
 //   warp 0      TMA producer: A (K-major, 128x64 box) and B (K-major 256x64
 //               box, or four MN-major 64x64 boxes) into a ring of 128B-swizzled
-//               shared-memory slots, one K-block each; a stage of two slots
-//               shares one full barrier (mbarrier transaction counts), each
-//               slot has its own empty barrier.
+//               shared-memory slots, one K-block each.  A stage (two slots on
+//               the CTA-pair loop, one on the single-CTA loop) shares one
+//               full barrier (mbarrier transaction counts); each slot has its
+//               own empty barrier.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators),
 //               then one lane issues tcgen05.mma (N=256, K=16) and commits
 //               each slot back to the producer and each finished
@@ -401,7 +402,7 @@ __device__ __noinline__ void drain_operand_loads(uint32_t bar_full0, uint32_t ow
     const uint32_t bar = bar_full0 + 8u * s;
     const uint32_t a0 = (own >> (2u * s * KPS)) & 3u;
     uint32_t at_a0 = 0, ahead = 0;
-    bool odd = false;
+    bool uneven = false;
     for (uint32_t h = 0; h < KPS; ++h) {
       const uint32_t sh = 2u * (s * KPS + h);
       if (((own >> sh) & 3u) == a0) ++at_a0;
@@ -412,10 +413,10 @@ __device__ __noinline__ void drain_operand_loads(uint32_t bar_full0, uint32_t ow
         else if (d == 1u)
           ++ahead;
         else if (d == 2u)
-          odd = true;  // not reachable when the producers keep in step
+          uneven = true;  // not reachable when the producers keep in step
       }
     }
-    if (odd) {
+    if (uneven) {
       late = true;
       continue;
     }
@@ -888,7 +889,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   ptx::tma_load_3d(sb + j * B_MN_BOX_BYTES, second ? &tm_b2 : &tm_b, fb, col, kb * BLOCK_K, zb);
                 }
               } else if (p.dual) {
-                // two 128-row K-major boxes, one per operand, stacked in the stage
+                // two 128-row K-major boxes, one per operand, stacked in the slot
                 ptx::tma_load_3d(sb, &tm_b, fb, kb * K_STEP, b_col, zb);
                 ptx::tma_load_3d(sb + (BLOCK_N / 2) * BLOCK_K * 2, &tm_b2, fb, kb * K_STEP, b_col, zb);
               } else {

@@ -46,7 +46,8 @@ __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// One non-blocking probe: true once the phase with parity `parity` is complete.
+// One probe (`try_wait`, which may suspend the thread for a short,
+// hardware-chosen time): true once the phase with parity `parity` is complete.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
