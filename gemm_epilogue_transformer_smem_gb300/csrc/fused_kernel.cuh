@@ -143,6 +143,9 @@ struct KernelParams {
   int32_t num_m_tiles, num_n_tiles, num_tiles, num_k_blocks;
   int32_t group_m;
   int32_t b_kn;  // 1: B stored K x N (MN-major operand)
+  // 1: the MN-major B map is 4-D (64 columns, K, 64-column blocks, batch),
+  // so one load fetches all of a K block's 64-column boxes of one operand
+  int32_t b_blk;
   int32_t dual;  // 1: accumulator columns alternate between B and B2 in 128-column blocks
   int32_t a_batched, b_batched;  // operand advances with the batch (else shared)
   int32_t row_blocks;            // row counters per batch
@@ -880,7 +883,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sb = sbase + L::OFF_B + stage * L::B_STAGE_BYTES + h * L::B_KB_BYTES;
             if (CG == 1) {
               ptx::tma_load_3d(sa, &tm_a, fb, kb * K_STEP, a_row, za);
-              if (p.b_kn) {
+              if (p.b_kn && p.b_blk) {
+                // with B2, blocks 0-1 come from B and 2-3 from B2
+                ptx::tma_load_4d(sb, &tm_b, fb, 0, kb * BLOCK_K, b_col / 64, zb);
+                if (p.dual) ptx::tma_load_4d(sb + 2 * B_MN_BOX_BYTES, &tm_b2, fb, 0, kb * BLOCK_K, b_col / 64, zb);
+              } else if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j) {
                   // with B2, boxes 0-1 come from B and 2-3 from B2
@@ -898,7 +905,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               const uint32_t fb0 = ptx::mapa_shared(fb, 0);
               ptx::tma_load_3d_cg2(sa, &tm_a, fb0, kb * K_STEP, a_row, za);
-              if (p.b_kn) {
+              if (p.b_kn && p.b_blk) {
+                ptx::tma_load_4d_cg2(sb, tmb_own, fb0, 0, kb * BLOCK_K, b_col / 64, zb);
+              } else if (p.b_kn) {
 #pragma unroll
                 for (int j = 0; j < L::B_COLS / 64; ++j)
                   ptx::tma_load_3d_cg2(sb + j * B_MN_BOX_BYTES, tmb_own, fb0, b_col + j * 64, kb * BLOCK_K, zb);

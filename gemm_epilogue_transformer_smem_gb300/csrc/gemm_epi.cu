@@ -188,6 +188,29 @@ gemm_epi_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* b
   return GEMM_EPI_OK;
 }
 
+// 4-D map of an MN-major (K x N) bf16 operand: 64 columns, K rows, the
+// 64-column blocks, batch.  A box of `blocks` blocks lands in shared memory as
+// that many consecutive 64 x 64 boxes, the layout the 3-D map fills with one
+// load per box.  Used only when N is a multiple of 64: a partial last block
+// would read past column N inside its 64-column extent.
+gemm_epi_status make_map_blocked(CUtensorMap* map, const void* base, uint64_t n, uint64_t k, uint64_t row_bytes,
+                                 uint32_t blocks, const char* what, uint64_t batch, uint64_t batch_bytes) {
+  if (batch_bytes == 0) {
+    batch = 1;
+    batch_bytes = row_bytes * (k > 0 ? k : 1);
+  }
+  cuuint64_t dims[4] = {64, k, n / 64, batch};
+  cuuint64_t strides[3] = {row_bytes, 128, batch_bytes};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(ge::BLOCK_K), blocks, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_EPI_ERR_CUDA, "cuTensorMapEncodeTiled(%s, blocked) failed with %d", what, static_cast<int>(r));
+  return GEMM_EPI_OK;
+}
+
 // Ops that write an output buffer: each may appear once per program.
 bool is_output_op(int c) {
   return c == GEMM_EPI_OP_AMAX || c == GEMM_EPI_OP_STORE_BF16 || c == GEMM_EPI_OP_STORE_E4M3 ||
@@ -534,10 +557,17 @@ gemm_epi_status prepare(const gemm_epi_plan& P, const gemm_epi_args& a, const De
     // rows one CTA stages from one operand.
     const int64_t b_cols = P.dual ? d.N / 2 : d.N;
     const uint32_t nk_rows = (P.dual || L.cg == 2) ? ge::BLOCK_N / 2 : ge::BLOCK_N;
+    // One load per K block and operand fetches the 64-column boxes this CTA
+    // stages from it: 2 (a CTA pair, or B and B2 apart) or 4.
+    k.b_blk = (k.b_kn && b_cols % 64 == 0) ? 1 : 0;
+    const uint32_t blk_boxes = (P.dual || L.cg == 2) ? 2u : 4u;
     for (int which = 0; which < (P.dual ? 2 : 1); ++which) {
       CUtensorMap* map = which == 0 ? &L.tb : &L.tb2;
       const void* base = which == 0 ? a.B : a.B2;
-      if (k.b_kn)
+      if (k.b_blk)
+        s = make_map_blocked(map, base, b_cols, d.K, d.ldb * 2, blk_boxes, which ? "B2" : "B", P.batch,
+                             k.b_batched ? d.batch_stride_b * 2 : 0);
+      else if (k.b_kn)
         s = make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, b_cols, d.K, d.ldb * 2, 64, ge::BLOCK_K,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, which ? "B2" : "B", P.batch,
                      k.b_batched ? d.batch_stride_b * 2 : 0);

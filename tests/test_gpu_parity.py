@@ -46,6 +46,9 @@ SMALL_SHAPES = [
     ("fp8in", 257, 528, 272),       # e4m3 operands, K tail of 16 (one 16-byte group)
     ("dswiglu", 300, 520, 200),     # SwiGLU backward: 1040 output columns, 8-column N tail
     ("drmsnorm", 300, 1000, 200),   # dy stored, column scale, row dot with x
+    # N a multiple of 64: B (K x N) comes through the 4-D map, one load per K block
+    ("swiglu", 260, 1024, 136),     # 4 N tiles, K tail of 8
+    ("fp8", 257, 576, 264),         # a last N tile of 64 columns (the rest of its blocks out of range)
 ]
 
 
