@@ -40,9 +40,10 @@ def _lib(cuda_lib):
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("shared_b", [False, True])
 @pytest.mark.parametrize("name", sorted(PROGRAMS))
-def test_batched_matches_per_batch_oracle(name, shared_b, variant):
+@pytest.mark.parametrize("N", [528, 512])  # 512: a K x N B comes through the 4-D map of 64-column blocks
+def test_batched_matches_per_batch_oracle(name, shared_b, variant, N):
     program, layout = PROGRAMS[name]
-    Bt, M, N, K = 3, 200, 528, 136
+    Bt, M, K = 3, 200, 136
     g = torch.Generator(device=DEV).manual_seed(41)
 
     def rnd(*shape, std=0.3):
